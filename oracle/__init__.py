@@ -1,0 +1,121 @@
+"""CPU oracle for GatedDeltaNet speculative verify + commit.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline leg may call it; the product path never does.  The arithmetic
+lives in ``gdn_oracle.c`` (plain C, fp64); this module only marshals arrays
+into it with ctypes.  It imports nothing from the CUDA library's package.
+
+Parity status of each part (what pins it) is listed in the tests'
+``test_oracle_pins.py`` docstrings.  Every function here is pinned by at
+least one invariant, closed form or brute-force case; the value-head to
+q/k-head mapping is a shared convention and is pinned only by the
+one-hot test that fixes which q/k head each value head reads.
+"""
+from __future__ import annotations
+
+import ctypes
+import time
+
+import numpy as np
+
+from . import build as _build
+
+BAD_SLOT, BAD_NROWS, BAD_ACCEPT = 1, 2, 4
+MUTATIONS = {
+    "conv_commit_early": 1,
+    "commit_a_rows": 2,
+    "verify_writes_live": 3,
+    "taps_reversed": 4,
+    "gqa_modulo": 5,
+    "o_before_update": 6,
+    "no_k_norm": 7,
+    "no_scale": 8,
+    "decay_after": 9,
+    "no_beta": 10,
+    "no_silu": 11,
+}
+DEFAULT_EPS = 1e-6
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("B", "R", "H_qk", "H_v", "d_k", "d_v", "W", "P")] + [
+        ("scale", ctypes.c_double),
+        ("l2_eps", ctypes.c_double),
+    ]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(str(_build.build()))
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.oracle_gdn_verify_commit.argtypes = [
+            ctypes.POINTER(_Dims), dp, dp, dp, dp, dp, dp, ip, ip, ip, dp, dp, dp, ctypes.c_int]
+        lib.oracle_gdn_verify_commit.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # torch tensor: widen exactly (bf16/fp32 -> fp64)
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a, ty):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ty))
+
+
+def verify_commit(layer: dict, *, commit: bool = True, snapshot: bool = False,
+                  accept_len=None, scale: float | None = None, l2_eps: float = DEFAULT_EPS,
+                  mutation: int | str = 0, requests=None) -> dict:
+    """Run the oracle on one layer call (the dict ``inputs.make_layer`` returns).
+
+    commit=False is a verify-only call (slots untouched).  ``requests``
+    restricts the call to a subset of request indices (for sampled checks at
+    full size); the other requests are treated as inactive.  Returns fp64
+    numpy arrays: o [B][R][H_v][d_v] (NaN where not produced), the slot pools
+    after the call, the status bits, and with snapshot=True the per-row
+    states and conv windows."""
+    spec = layer["spec"]
+    B, R, C, W = spec.B, spec.R, spec.C, spec.W
+    dims = _Dims(B, R, spec.H_qk, spec.H_v, spec.d_k, spec.d_v, W, spec.pool_slots,
+                 spec.d_k ** -0.5 if scale is None else scale, l2_eps)
+    x, g, beta = _f64(layer["x"]), _f64(layer["g"]), _f64(layer["beta"])
+    conv_w = _f64(layer["conv_w"])
+    conv_state = _f64(layer["conv_state"]).copy()
+    ssm_state = _f64(layer["ssm_state"]).copy()
+    slots = _i32(layer["slot_ids"])
+    n_rows = _i32(layer["n_rows"]).copy()
+    if requests is not None:
+        keep = np.zeros(B, dtype=bool)
+        keep[np.asarray(list(requests), dtype=np.int64)] = True
+        n_rows[~keep] = 0
+    acc = _i32(layer["accept_len"] if accept_len is None else accept_len) if commit else None
+    o = np.full((B, R, spec.H_v, spec.d_v), np.nan)
+    snap_S = np.full((B, R) + ssm_state.shape[1:], np.nan) if snapshot else None
+    snap_cs = np.full((B, R, C, W - 1), np.nan) if snapshot else None
+    mut = MUTATIONS[mutation] if isinstance(mutation, str) else int(mutation)
+    dp, ip = ctypes.c_double, ctypes.c_int
+    t0 = time.perf_counter()
+    status = _load().oracle_gdn_verify_commit(
+        ctypes.byref(dims), _ptr(x, dp), _ptr(g, dp), _ptr(beta, dp), _ptr(conv_w, dp),
+        _ptr(conv_state, dp), _ptr(ssm_state, dp), _ptr(slots, ip), _ptr(n_rows, ip),
+        _ptr(acc, ip), _ptr(o, dp), _ptr(snap_S, dp), _ptr(snap_cs, dp), mut)
+    seconds = time.perf_counter() - t0
+    out = {"o": o, "ssm_state": ssm_state, "conv_state": conv_state, "status": int(status),
+           "seconds": seconds}
+    if snapshot:
+        out["snap_S"], out["snap_cs"] = snap_S, snap_cs
+    return out
