@@ -1,0 +1,368 @@
+"""Benchmark: GatedDeltaNet verify + commit, verified rows/s and HBM GB/s.
+
+One step = one pass of the whole verify + commit path over a 36-layer stack
+of Qwen3.5-shaped GDN layers (B = 16 requests, k = 3 drafts -> 4 rows each,
+H_qk = 16, H_v = 32, d_k = d_v = 128, bf16 inputs, fp32 state), one layer
+call after another on one stream.  Every step moves ~2.5 GB, far more than
+the 126 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--mode fused|replay|snapshot]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica of the stack (weak scaling, no collective on the data path); the
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decode_gateddeltanet_gb300.inputs import STACK, make_layer, spec_bytes, workload_layers  # noqa: E402
+
+METRIC = "GDN verify+commit verified rows/sec and achieved HBM GB/s (% of peak), 1 GB300"
+UNIT = "rows/s"
+KERNEL_SRC = os.path.join(ROOT, "speculative_decode_gateddeltanet_gb300", "csrc", "gdn_spec.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(workload: str, mode: str):
+    """dram bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    h = kernel_source_hash()
+    for line in open(TRAFFIC_FILE):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[:3] == [workload, mode, h]:
+            return float(parts[3])
+    return None
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+
+    rank, local = int(os.environ["RANK"]), int(os.environ.get("LOCAL_RANK", "0"))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, ws: int) -> float:
+    if ws <= 1:
+        return value
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ CUDA arm
+def build_stack(layers: int, device: str):
+    from speculative_decode_gateddeltanet_gb300 import gdn
+
+    host, devs = [], []
+    for spec, seed in workload_layers(STACK, layers=layers):
+        layer = make_layer(spec, seed)
+        host.append(layer)
+        devs.append(gdn.DeviceLayer(layer, device, snapshot=False))
+    return host, devs
+
+
+def run_cuda(args, rank, ws, local):
+    from speculative_decode_gateddeltanet_gb300 import build as pkg_build
+
+    pkg_build.build()
+    from speculative_decode_gateddeltanet_gb300 import gdn
+
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    host, devs = build_stack(args.layers, device)
+    spec = host[0]["spec"]
+    if args.mode == "snapshot":
+        for d in devs:
+            d.scratch_S = torch.empty((spec.B, spec.R, spec.H_v, spec.d_v, spec.d_k), device=device)
+            d.scratch_cs = torch.empty((spec.B, spec.R, spec.C, spec.W - 1), dtype=d.x.dtype, device=device)
+    cargs = [d.args() for d in devs]
+    stream = torch.cuda.Stream(device)
+    sp = stream.cuda_stream
+
+    def step():
+        if args.mode == "fused":
+            for a in cargs:
+                gdn.gdn_verify_commit(a, sp)
+        else:
+            m = gdn.REPLAY if args.mode == "replay" else gdn.SNAPSHOT
+            for a in cargs:
+                gdn.gdn_verify(a, m, sp)
+                gdn.gdn_commit(a, m, sp)
+
+    launches_per_step = len(cargs) * (1 if args.mode == "fused" else 2)
+    rows_per_step = sum(int(h["n_rows"].clamp(min=0).sum()) for h in host)
+    bytes_per_step = sum(spec_bytes(h["spec"], h["n_rows"]) for h in host)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region ----
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.4)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
+    ms_step = ms / args.steps
+    value = rows_per_step * ws / (ms_step / 1e3)
+    for d in devs:
+        assert int(d.status.item()) == 0, "device status bits set"
+
+    # ---- end to end: pinned host inputs -> device -> call -> o back to host ----
+    host_in = []
+    for h in host:
+        host_in.append({k: h[k].pin_memory() for k in ("x", "g", "beta", "slot_ids", "n_rows", "accept_len")})
+    host_o = [torch.empty(d.o.shape, dtype=d.o.dtype).pin_memory() for d in devs]
+    h2d = sum(t.numel() * t.element_size() for hi in host_in for t in hi.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_o)
+
+    def e2e_step():
+        for hi, d, a, ho in zip(host_in, devs, cargs, host_o):
+            for k, t in hi.items():
+                getattr(d, k).copy_(t, non_blocking=True)
+            if args.mode == "fused":
+                gdn.gdn_verify_commit(a, sp)
+            else:
+                m = gdn.REPLAY if args.mode == "replay" else gdn.SNAPSHOT
+                gdn.gdn_verify(a, m, sp)
+                gdn.gdn_commit(a, m, sp)
+            ho.copy_(d.o, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), ws) / e2e_steps
+
+    peak, peak_kind = hbm_peak()
+    per_launch_bytes = bytes_per_step / len(cargs)
+    launch_s = ms_step / 1e3 / launches_per_step
+    achieved = per_launch_bytes / launch_s / 1e9 if args.mode == "fused" else bytes_per_step / (ms_step / 1e3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": spec.name, "layers": len(cargs), "B": spec.B, "k": spec.k, "rows_per_layer":
+                   rows_per_step // len(cargs), "H_qk": spec.H_qk, "H_v": spec.H_v, "d_k": spec.d_k,
+                   "d_v": spec.d_v, "storage": "bf16 x/conv, fp32 g/beta/state/o", "mode": args.mode,
+                   "l2": "inputs larger than L2: each step streams %.2f GB over %d distinct layers"
+                         % (bytes_per_step / 1e9, len(cargs))},
+        "hbm_gbs": round(bytes_per_step * ws / (ms_step / 1e3) / 1e9, 1),
+        "bytes_per_row": round(bytes_per_step / rows_per_step),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "kernel": "rows_kernel<128,bf16,%s>" % args.mode,
+                     "traffic": measured_traffic(spec.name, args.mode),
+                     "algorithmic_bytes_per_launch": round(per_launch_bytes)},
+        "e2e": {"value": round(rows_per_step * ws / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    return out
+
+
+# ------------------------------------------------------------ oracle arm
+def oracle_rows_per_second(budget_s: float, max_layers: int = 36):
+    """Time the oracle on whole layers of the stack until the budget is used."""
+    import oracle
+
+    rows, secs, layers = 0, 0.0, 0
+    for spec, seed in workload_layers(STACK, layers=max_layers):
+        layer = make_layer(spec, seed)
+        r = oracle.verify_commit(layer)
+        rows += int(layer["n_rows"].clamp(min=0).sum())
+        secs += r["seconds"]
+        layers += 1
+        if secs >= budget_s:
+            break
+    return rows, secs, layers
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    rows, secs, layers = oracle_rows_per_second(budget_s)
+    return {"value": round(rows / secs, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 C oracle, single thread, fused verify+commit of {layers} whole layers "
+                      f"({rows} rows) of the 36-layer B=16 k=3 stack, {secs:.1f} s"}
+
+
+def run_reference(args, rank, ws):
+    """The oracle as it stands, on the host cores, on the same workload."""
+    import oracle
+
+    if rank != 0:
+        return None
+    spec, seed = workload_layers(STACK, layers=1)[0]
+    layer = make_layer(spec, seed)
+    r = oracle.verify_commit(layer, requests=[0])
+    t_req = max(r["seconds"], 1e-4)
+    budget = 150.0
+    per_step = max(1, min(spec.B, int(budget / (args.steps + args.warmup) / t_req)))
+    reqs = list(range(per_step))
+    rows_step = int(layer["n_rows"][:per_step].clamp(min=0).sum())
+    for _ in range(args.warmup):
+        oracle.verify_commit(layer, requests=reqs)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle.verify_commit(layer, requests=reqs)["seconds"]
+    ms_step = t / args.steps * 1e3
+    value = rows_step / (ms_step / 1e3)
+    sample = (f"fp64 C oracle, single thread: {per_step} of the {spec.B} requests of one layer of the "
+              f"36-layer B=16 k=3 stack per step ({rows_step} rows)")
+    return {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": spec.name, "layers": 36, "B": spec.B, "k": spec.k, "mode": "fused"},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["fused", "replay", "snapshot"], default="fused")
+    ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        out = run_reference(args, rank, ws)
+    else:
+        out = run_cuda(args, rank, ws, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,143 @@
+/*
+ * gdnspec: target-side verify and commit of one GatedDeltaNet (GDN)
+ * linear-attention layer for MTP speculative decoding, on NVIDIA GB300
+ * (sm_103a).  C ABI; every buffer belongs to the caller.
+ *
+ * The operation.  A verify step scores, per request, the k+1 rows
+ * [pending, d1..dk] in one pass [FreeToken #844 "MTP drafts for Qwen3.5
+ * family + Flash-Next", Design; FreeToken #828 "Speculative decoding: MTP and
+ * DFlash", Design: "a uniform extend of k+1 rows per request"].  Each row runs
+ * one GDN decode step:
+ *   window_t[c] = last W entries of [conv_state[c][0..W-2], x_0[c] .. x_t[c]]
+ *   y_t[c]      = SiLU(sum_j conv_w[c][j] * window_t[c][j])   (tap W-1 = newest)
+ *   q, k        = per q/k head  y / sqrt(sum y^2 + l2_eps),  v = v block of y
+ *   per value head h, with q/k head h / (H_v / H_qk):
+ *     S_t = exp(g_t) S_{t-1} + beta_t (v - exp(g_t) S_{t-1} k) k^T
+ *     o_t = scale * S_t q
+ * The GDN state is only read during the verify; the commit then makes each
+ * request's slot hold the state after its accepted rows [FreeToken #828,
+ * Design], with the conv window "as it stands after the accepted rows"
+ * [FreeToken #844, Flash-Next target verify].  accept_len = a counts accepted
+ * drafts; the commit covers rows 0..a (a+1 tokens, the pages' "accept
+ * length", FreeToken #844, End-to-end).  The verify may also snapshot every
+ * row's state so the commit is a copy [LightLLM #1330 "Qwen3.5 / Qwen3.5-MoE
+ * MTP speculative decoding", Summary: widened verify state, snapshot/restore];
+ * or verify and commit run in one pass [lmdeploy #5006 "speculative decoding
+ * for TurboMind", Verification path: verify-and-commit kernel mode].
+ *
+ * Layouts (row-major, C = 2*H_qk*d_k + H_v*d_v, channels [q heads|k heads|v heads]):
+ *   x           [B][R][C]             in_dtype   pre-conv rows; row t < n_rows[b] valid
+ *   g, beta     [B][R][H_v]           fp32       log-decay (exp(g) is the decay), write strength
+ *   conv_w      [C][W]                in_dtype   depthwise taps, tap W-1 multiplies the newest row
+ *   conv_state  [pool_slots][C][W-1]  in_dtype   committed window, oldest column first
+ *   ssm_state   [pool_slots][H_v][d_v][d_k] fp32 committed state S (d_v x d_k per head)
+ *   slot_ids, n_rows, accept_len [B]  int32      request -> slot; valid rows (0 = inactive);
+ *                                                accepted drafts, 0..n_rows-1
+ *   o           [B][R][H_v][d_v]      fp32       verify output; only rows t < n_rows[b] of
+ *                                                active requests are written
+ *   scratch_S   [B][R][H_v][d_v][d_k] fp32       snapshot mode: state after row t
+ *   scratch_cs  [B][R][C][W-1]        in_dtype   snapshot mode: conv window after row t
+ *   counters    [B*H_qk]              int32      zero before the first call; every call that
+ *                                                commits in replay or fused form leaves it zero
+ *   status      [1]                   int32      device word; error bits are OR-ed in, never cleared
+ *
+ * Supported: W = 4; d_k in {16, 32, 64, 128}; d_v a multiple of 16 (d_k = 16)
+ * or of 32 (d_k >= 32); H_v a multiple of H_qk; 1 <= R <= 16.
+ *
+ * Ownership, synchronisation.  All pointers are device pointers owned by the
+ * caller; the library keeps none after a call returns, allocates nothing,
+ * and never synchronises the stream.  Calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream).  Active requests must
+ * use distinct slots; two calls that touch the same slots or counters must
+ * not run concurrently.  In replay mode the verify and the commit must see
+ * the same x, g, beta, conv_w and slot contents.
+ *
+ * Errors.  Host return codes: GDN_OK, or GDN_ERR_* for arguments the host
+ * can check (null pointers, shapes, alignment; nothing is launched) and for a
+ * failed launch.  Values only the device sees are not trapped: a request whose
+ * slot is outside [0, pool_slots) or whose n_rows is outside [0, R] is skipped
+ * entirely (nothing written for it) and sets GDN_STATUS_BAD_SLOT /
+ * GDN_STATUS_BAD_NROWS in *status; an accept_len outside [0, n_rows-1]
+ * skips that request's commit (its o is still written) and sets
+ * GDN_STATUS_BAD_ACCEPT.  status may be NULL (no bits recorded).
+ */
+#ifndef GDNSPEC_H
+#define GDNSPEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_API __attribute__((visibility("default")))
+
+enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size  */
+  GDN_ERR_UNSUPPORTED = 2, /* W, d_k, d_v, R or dtype outside the set above */
+  GDN_ERR_MISALIGNED = 3,  /* a pointer below its required alignment        */
+  GDN_ERR_LAUNCH = 4       /* the CUDA launch failed                        */
+};
+
+enum { GDN_STATUS_BAD_SLOT = 1, GDN_STATUS_BAD_NROWS = 2, GDN_STATUS_BAD_ACCEPT = 4 };
+enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
+enum { GDN_REPLAY = 0, GDN_SNAPSHOT = 1 };
+
+typedef struct gdn_args {
+  int32_t B;          /* requests (0 = nothing to do)                          */
+  int32_t R;          /* rows per request in x/g/beta/o (k_max + 1)            */
+  int32_t H_qk;       /* q/k heads                                             */
+  int32_t H_v;        /* value heads                                           */
+  int32_t d_k;        /* q/k head dim = state columns                          */
+  int32_t d_v;        /* v head dim = state rows                               */
+  int32_t W;          /* conv width, must be 4                                 */
+  int32_t pool_slots; /* slots in conv_state / ssm_state                       */
+  int32_t in_dtype;   /* GDN_DTYPE_* of x, conv_w, conv_state, scratch_cs      */
+  float scale;        /* o = scale * S q (usually d_k^-1/2), finite            */
+  float l2_eps;       /* >= 0, added to sum y^2 before the square root         */
+  int32_t flags;      /* must be 0                                             */
+  const void* x;      /* 16-byte aligned pointers: ssm_state, scratch_S, o;     */
+  const float* g;     /* the rest need their element's natural alignment        */
+  const float* beta;
+  const void* conv_w;
+  void* conv_state;
+  float* ssm_state;
+  const int32_t* slot_ids;
+  const int32_t* n_rows;
+  const int32_t* accept_len; /* commit and fused calls only                    */
+  float* o;                  /* verify and fused calls only                    */
+  float* scratch_S;          /* snapshot mode only                             */
+  void* scratch_cs;          /* snapshot mode only                             */
+  int32_t* counters;         /* replay commit and fused calls only             */
+  int32_t* status;           /* may be NULL                                    */
+} gdn_args;
+
+/* Verify: for every active request, run rows 0..n_rows-1 from its slot's
+ * committed state and write o.  Never writes conv_state or ssm_state.
+ * mode GDN_SNAPSHOT also writes, per row t, the state and conv window a
+ * commit at accept_len = t would leave into scratch_S / scratch_cs[b][t]
+ * (the widened verify state).  Needs: x, g, beta, conv_w, conv_state,
+ * ssm_state, slot_ids, n_rows, o (+ scratch_S, scratch_cs in snapshot mode). */
+GDN_API int gdn_verify(const gdn_args* args, int mode, void* stream);
+
+/* Commit: make slot slot_ids[b] hold the state and conv window after rows
+ * 0..accept_len[b] of request b.  mode GDN_REPLAY reruns those rows from the
+ * committed state (same arithmetic as the verify, so the result equals a
+ * fused call bit for bit) and needs the verify's inputs plus accept_len and
+ * counters; mode GDN_SNAPSHOT copies row accept_len[b] of a snapshot verify's
+ * scratch and needs slot_ids, n_rows, accept_len, scratch_S, scratch_cs. */
+GDN_API int gdn_commit(const gdn_args* args, int mode, void* stream);
+
+/* Verify and commit in one pass over the state: writes o for every valid
+ * row and, at row accept_len[b], the slot.  Each state byte is read once and
+ * written once.  Needs everything gdn_verify needs plus accept_len, counters. */
+GDN_API int gdn_verify_commit(const gdn_args* args, void* stream);
+
+/* Static description of a return code (never NULL). */
+GDN_API const char* gdn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDNSPEC_H */

@@ -1,0 +1,144 @@
+"""Python binding of ``libgdnspec`` (the C ABI in ``include/gdnspec.h``).
+
+Argument marshalling only: every step of the verify and commit runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  If the
+library has not been built the import fails; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libgdnspec.so"
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH = 0, 1, 2, 3, 4
+STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT = 1, 2, 4
+BF16, F32 = 0, 1
+REPLAY, SNAPSHOT = 0, 1
+
+_I32, _F32, _P = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+
+
+class GdnArgs(ctypes.Structure):
+    """Mirror of ``gdn_args``."""
+
+    _fields_ = [
+        ("B", _I32), ("R", _I32), ("H_qk", _I32), ("H_v", _I32), ("d_k", _I32), ("d_v", _I32),
+        ("W", _I32), ("pool_slots", _I32), ("in_dtype", _I32), ("scale", _F32), ("l2_eps", _F32),
+        ("flags", _I32),
+        ("x", _P), ("g", _P), ("beta", _P), ("conv_w", _P), ("conv_state", _P), ("ssm_state", _P),
+        ("slot_ids", _P), ("n_rows", _P), ("accept_len", _P), ("o", _P), ("scratch_S", _P),
+        ("scratch_cs", _P), ("counters", _P), ("status", _P),
+    ]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+if not LIB_PATH.exists():
+    raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() "
+                      "(or python -m speculative_decode_gateddeltanet_gb300.build)")
+_lib = ctypes.CDLL(str(LIB_PATH))
+_lib.gdn_verify.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int, _P]
+_lib.gdn_commit.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int, _P]
+_lib.gdn_verify_commit.argtypes = [ctypes.POINTER(GdnArgs), _P]
+for _f in (_lib.gdn_verify, _lib.gdn_commit, _lib.gdn_verify_commit):
+    _f.restype = ctypes.c_int
+_lib.gdn_strerror.argtypes = [ctypes.c_int]
+_lib.gdn_strerror.restype = ctypes.c_char_p
+
+
+def strerror(code: int) -> str:
+    return _lib.gdn_strerror(code).decode()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return stream or None
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OK:
+        raise GdnError(rc, where)
+
+
+def gdn_verify(args: GdnArgs, mode: int = REPLAY, stream=None) -> None:
+    _check(_lib.gdn_verify(ctypes.byref(args), mode, _stream(stream)), "gdn_verify")
+
+
+def gdn_commit(args: GdnArgs, mode: int = REPLAY, stream=None) -> None:
+    _check(_lib.gdn_commit(ctypes.byref(args), mode, _stream(stream)), "gdn_commit")
+
+
+def gdn_verify_commit(args: GdnArgs, stream=None) -> None:
+    _check(_lib.gdn_verify_commit(ctypes.byref(args), _stream(stream)), "gdn_verify_commit")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_qk: int,
+              accept_len=None, o=None, scratch_S=None, scratch_cs=None, counters=None,
+              status=None, scale: float | None = None, l2_eps: float = 1e-6) -> GdnArgs:
+    """Fill a GdnArgs from tensors laid out as ``include/gdnspec.h`` states.
+
+    Shapes are read from x [B][R][C], ssm_state [P][H_v][d_v][d_k] and
+    conv_w [C][W]; the tensors must stay alive while the call runs."""
+    B, R, _ = x.shape
+    P, H_v, d_v, d_k = ssm_state.shape
+    W = conv_w.shape[1]
+    if x.dtype == torch.bfloat16:
+        dt = BF16
+    elif x.dtype == torch.float32:
+        dt = F32
+    else:
+        raise TypeError(f"unsupported input dtype {x.dtype}")
+    return GdnArgs(
+        B=B, R=R, H_qk=H_qk, H_v=H_v, d_k=d_k, d_v=d_v, W=W, pool_slots=P, in_dtype=dt,
+        scale=d_k ** -0.5 if scale is None else scale, l2_eps=l2_eps, flags=0,
+        x=_ptr(x), g=_ptr(g), beta=_ptr(beta), conv_w=_ptr(conv_w), conv_state=_ptr(conv_state),
+        ssm_state=_ptr(ssm_state), slot_ids=_ptr(slot_ids), n_rows=_ptr(n_rows),
+        accept_len=_ptr(accept_len), o=_ptr(o), scratch_S=_ptr(scratch_S),
+        scratch_cs=_ptr(scratch_cs), counters=_ptr(counters), status=_ptr(status))
+
+
+class DeviceLayer:
+    """One layer call's buffers on a CUDA device, plus the call's outputs.
+
+    Built from a dict of CPU tensors (the layout ``inputs.make_layer`` uses).
+    ``o`` is filled with NaN so rows a call must not write stay visibly
+    untouched; ``counters`` and ``status`` start at zero."""
+
+    KEYS = ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows", "accept_len")
+
+    def __init__(self, layer: dict, device="cuda", snapshot: bool = False, scale=None,
+                 l2_eps: float = 1e-6):
+        self.spec = layer["spec"]
+        s = self.spec
+        for k in self.KEYS:
+            setattr(self, k, layer[k].to(device).contiguous())
+        self.o = torch.full((s.B, s.R, s.H_v, s.d_v), float("nan"), device=device)
+        self.counters = torch.zeros(s.B * s.H_qk, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.scratch_S = self.scratch_cs = None
+        if snapshot:
+            self.scratch_S = torch.empty((s.B, s.R, s.H_v, s.d_v, s.d_k), device=device)
+            self.scratch_cs = torch.empty((s.B, s.R, s.C, s.W - 1), dtype=self.x.dtype, device=device)
+        self.scale, self.l2_eps = scale, l2_eps
+
+    def args(self) -> GdnArgs:
+        return make_args(x=self.x, g=self.g, beta=self.beta, conv_w=self.conv_w,
+                         conv_state=self.conv_state, ssm_state=self.ssm_state,
+                         slot_ids=self.slot_ids, n_rows=self.n_rows, accept_len=self.accept_len,
+                         o=self.o, scratch_S=self.scratch_S, scratch_cs=self.scratch_cs,
+                         counters=self.counters, status=self.status, H_qk=self.spec.H_qk,
+                         scale=self.scale, l2_eps=self.l2_eps)

@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, the ctypes mirror matches the C struct layout, and host-side argument
+checks reject bad calls before anything is launched."""
+from __future__ import annotations
+
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "gdnspec.h"
+
+
+def declared_symbols():
+    text = HEADER.read_text()
+    return re.findall(r"^GDN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_strerror"}
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    lib = ctypes.CDLL(str(cuda_lib.LIB_PATH))
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", str(cuda_lib.LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(declared_symbols()) <= exported
+    assert not any(s.startswith("_ZN7gdnspec") for s in exported), "internal symbols leak"
+
+
+def test_struct_layout_matches_header(cuda_lib, tmp_path):
+    fields = [f[0] for f in cuda_lib.GdnArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdnspec.h"\nint main(void){\n'
+                   + 'printf("%zu\\n", sizeof(gdn_args));\n'
+                   + "".join(f'printf("%zu\\n", offsetof(gdn_args, {f}));\n' for f in fields)
+                   + "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", str(HEADER.parent), str(src), "-o", str(exe)], check=True)
+    vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(cuda_lib.GdnArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(cuda_lib.GdnArgs, f).offset == off, f
+
+
+def test_strerror_covers_codes(cuda_lib):
+    for code in range(5):
+        assert cuda_lib.strerror(code) and "unknown" not in cuda_lib.strerror(code)
+    assert "unknown" in cuda_lib.strerror(99)
+
+
+FAKE = 1 << 20  # a 16-byte aligned stand-in address; never dereferenced on these paths
+
+
+def good_args(gdn, **over):
+    a = gdn.GdnArgs(B=2, R=4, H_qk=16, H_v=32, d_k=128, d_v=128, W=4, pool_slots=4,
+                    in_dtype=gdn.BF16, scale=128 ** -0.5, l2_eps=1e-6, flags=0)
+    for f in ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows",
+              "accept_len", "o", "scratch_S", "scratch_cs", "counters"):
+        setattr(a, f, FAKE)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+CASES = [
+    ("negative B", dict(B=-1), 1),
+    ("zero rows", dict(R=0), 1),
+    ("too many rows", dict(R=17), 2),
+    ("conv width", dict(W=3), 2),
+    ("d_k", dict(d_k=96), 2),
+    ("d_v not a multiple of the block rows", dict(d_v=48), 2),
+    ("H_v % H_qk", dict(H_v=24), 2),
+    ("dtype", dict(in_dtype=7), 2),
+    ("flags", dict(flags=1), 1),
+    ("negative eps", dict(l2_eps=-1.0), 1),
+    ("nan scale", dict(scale=float("nan")), 1),
+    ("null x", dict(x=None), 1),
+    ("null state", dict(ssm_state=None), 1),
+    ("null o", dict(o=None), 1),
+    ("null accept_len", dict(accept_len=None), 1),
+    ("null counters", dict(counters=None), 1),
+    ("misaligned state", dict(ssm_state=FAKE + 4), 3),
+    ("misaligned o", dict(o=FAKE + 8), 3),
+    ("misaligned x", dict(x=FAKE + 1), 3),
+    ("misaligned status", dict(status=FAKE + 2), 3),
+    ("too many requests", dict(B=70000), 2),
+]
+
+
+@pytest.mark.parametrize("what,over,code", CASES, ids=[c[0] for c in CASES])
+def test_fused_rejects_bad_arguments(cuda_lib, what, over, code):
+    a = good_args(cuda_lib, **over)
+    rc = cuda_lib._lib.gdn_verify_commit(ctypes.byref(a), None)
+    assert rc == code, (what, cuda_lib.strerror(rc))
+
+
+def test_mode_specific_requirements(cuda_lib):
+    lib, g = cuda_lib._lib, cuda_lib
+    # verify needs no accept_len / counters; snapshot verify needs scratch
+    a = good_args(g, B=0, accept_len=None, counters=None)
+    assert lib.gdn_verify(ctypes.byref(a), g.REPLAY, None) == g.OK
+    a = good_args(g, scratch_S=None)
+    assert lib.gdn_verify(ctypes.byref(a), g.SNAPSHOT, None) == g.ERR_INVALID_ARG
+    assert lib.gdn_verify(ctypes.byref(a), 5, None) == g.ERR_INVALID_ARG
+    # snapshot commit needs scratch and accept_len, not x
+    a = good_args(g, x=None, scratch_cs=None)
+    assert lib.gdn_commit(ctypes.byref(a), g.SNAPSHOT, None) == g.ERR_INVALID_ARG
+    a = good_args(g, B=0, x=None)
+    assert lib.gdn_commit(ctypes.byref(a), g.SNAPSHOT, None) == g.OK
+    # replay commit needs counters
+    a = good_args(g, counters=None)
+    assert lib.gdn_commit(ctypes.byref(a), g.REPLAY, None) == g.ERR_INVALID_ARG
+    assert lib.gdn_verify_commit(None, None) == g.ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(cuda_lib):
+    a = good_args(cuda_lib, B=0)
+    for call in (lambda: cuda_lib._lib.gdn_verify_commit(ctypes.byref(a), None),
+                 lambda: cuda_lib._lib.gdn_verify(ctypes.byref(a), 0, None),
+                 lambda: cuda_lib._lib.gdn_commit(ctypes.byref(a), 0, None)):
+        assert call() == cuda_lib.OK
+
+
+def test_binding_raises_on_error(cuda_lib):
+    a = good_args(cuda_lib, d_k=96)
+    with pytest.raises(cuda_lib.GdnError) as e:
+        cuda_lib.gdn_verify_commit(a, stream=0)
+    assert e.value.code == cuda_lib.ERR_UNSUPPORTED
+
+
+def test_product_never_imports_the_oracle():
+    pkg = ROOT / "speculative_decode_gateddeltanet_gb300"
+    for p in list(pkg.rglob("*.py")) + list(pkg.rglob("*.cu")) + list(pkg.rglob("*.h")):
+        text = p.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, p
+        assert "gdn_oracle" not in text, p
