@@ -287,22 +287,22 @@ def oracle_rows_per_second(budget_s: float, max_layers: int = 36):
     import oracle
 
     rows, secs, layers = 0, 0.0, 0
-    for spec, seed in workload_layers(STACK, layers=max_layers):
+    stack = workload_layers(STACK, layers=max_layers)
+    while secs < budget_s:
+        spec, seed = stack[layers % len(stack)]
         layer = make_layer(spec, seed)
         r = oracle.verify_commit(layer)
         rows += int(layer["n_rows"].clamp(min=0).sum())
         secs += r["seconds"]
         layers += 1
-        if secs >= budget_s:
-            break
     return rows, secs, layers
 
 
 def cpu_baseline(budget_s: float = 12.0):
     rows, secs, layers = oracle_rows_per_second(budget_s)
     return {"value": round(rows / secs, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"fp64 C oracle, single thread, fused verify+commit of {layers} whole layers "
-                      f"({rows} rows) of the 36-layer B=16 k=3 stack, {secs:.1f} s"}
+            "sample": f"fp64 C oracle, single thread, fused verify+commit of {layers} whole layer calls "
+                      f"({rows} rows) cycling over the 36-layer B=16 k=3 stack, {secs:.1f} s"}
 
 
 def run_reference(args, rank, ws):

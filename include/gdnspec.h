@@ -37,8 +37,9 @@
  *                                                active requests are written
  *   scratch_S   [B][R][H_v][d_v][d_k] fp32       snapshot mode: state after row t
  *   scratch_cs  [B][R][C][W-1]        in_dtype   snapshot mode: conv window after row t
- *   counters    [B*H_qk]              int32      zero before the first call; every call that
- *                                                commits in replay or fused form leaves it zero
+ *   counters    [B*H_qk*GDN_COUNTERS_PER_QK_HEAD] int32  zero before the first call; every
+ *                                                call that commits in replay or fused form
+ *                                                leaves it zero
  *   status      [1]                   int32      device word; error bits are OR-ed in, never cleared
  *
  * Supported: W = 4; d_k in {16, 32, 64, 128}; d_v a multiple of 16 (d_k = 16)
@@ -59,7 +60,10 @@
  * entirely (nothing written for it) and sets GDN_STATUS_BAD_SLOT /
  * GDN_STATUS_BAD_NROWS in *status; an accept_len outside [0, n_rows-1]
  * skips that request's commit (its o is still written) and sets
- * GDN_STATUS_BAD_ACCEPT.  status may be NULL (no bits recorded).
+ * GDN_STATUS_BAD_ACCEPT.  A kernel never spins without bound: if one of its
+ * staging copies does not land within a bounded wait, the blocks that depend
+ * on it write nothing and GDN_STATUS_TIMEOUT is set.  status may be NULL (no
+ * bits recorded).
  */
 #ifndef GDNSPEC_H
 #define GDNSPEC_H
@@ -72,6 +76,9 @@ extern "C" {
 
 #define GDN_API __attribute__((visibility("default")))
 
+/* Length of `counters` per (request, q/k head). */
+#define GDN_COUNTERS_PER_QK_HEAD 8
+
 enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size  */
@@ -80,7 +87,13 @@ enum {
   GDN_ERR_LAUNCH = 4       /* the CUDA launch failed                        */
 };
 
-enum { GDN_STATUS_BAD_SLOT = 1, GDN_STATUS_BAD_NROWS = 2, GDN_STATUS_BAD_ACCEPT = 4 };
+enum {
+  GDN_STATUS_BAD_SLOT = 1,   /* slot outside [0, pool_slots): request skipped         */
+  GDN_STATUS_BAD_NROWS = 2,  /* n_rows outside [0, R]: request skipped                */
+  GDN_STATUS_BAD_ACCEPT = 4, /* accept_len outside [0, n_rows-1]: commit skipped      */
+  GDN_STATUS_TIMEOUT = 8     /* a staging copy did not complete within the kernel's
+                                bounded wait: that block wrote nothing                */
+};
 enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
 enum { GDN_REPLAY = 0, GDN_SNAPSHOT = 1 };
 
@@ -97,8 +110,8 @@ typedef struct gdn_args {
   float scale;        /* o = scale * S q (usually d_k^-1/2), finite            */
   float l2_eps;       /* >= 0, added to sum y^2 before the square root         */
   int32_t flags;      /* must be 0                                             */
-  const void* x;      /* 16-byte aligned pointers: ssm_state, scratch_S, o;     */
-  const float* g;     /* the rest need their element's natural alignment        */
+  const void* x;      /* 16-byte aligned: x, conv_w, conv_state, ssm_state, o,  */
+  const float* g;     /* scratch_S, scratch_cs; 4-byte: g, beta, int32 arrays   */
   const float* beta;
   const void* conv_w;
   void* conv_state;

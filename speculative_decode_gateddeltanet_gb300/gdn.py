@@ -16,6 +16,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libgdnspec.so"
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH = 0, 1, 2, 3, 4
 STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT = 1, 2, 4
 BF16, F32 = 0, 1
+COUNTERS_PER_QK_HEAD = 8
 REPLAY, SNAPSHOT = 0, 1
 
 _I32, _F32, _P = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
@@ -127,7 +128,7 @@ class DeviceLayer:
         for k in self.KEYS:
             setattr(self, k, layer[k].to(device).contiguous())
         self.o = torch.full((s.B, s.R, s.H_v, s.d_v), float("nan"), device=device)
-        self.counters = torch.zeros(s.B * s.H_qk, dtype=torch.int32, device=device)
+        self.counters = torch.zeros(s.B * s.H_qk * COUNTERS_PER_QK_HEAD, dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.scratch_S = self.scratch_cs = None
         if snapshot:
