@@ -37,9 +37,9 @@
  *                                                active requests are written
  *   scratch_S   [B][R][H_v][d_v][d_k] fp32       snapshot mode: state after row t
  *   scratch_cs  [B][R][C][W-1]        in_dtype   snapshot mode: conv window after row t
- *   counters    [B*H_qk*GDN_COUNTERS_PER_QK_HEAD] int32  zero before the first call; every
- *                                                call that commits in replay or fused form
- *                                                leaves it zero
+ *   work        gdn_work_bytes(args) bytes       the call's own scratch: per row the
+ *                                                normalised q and k of every q/k head, v,
+ *                                                and k.q; contents on entry do not matter
  *   status      [1]                   int32      device word; error bits are OR-ed in, never cleared
  *
  * Supported: W = 4; d_k in {16, 32, 64, 128}; d_v a multiple of 16 (d_k = 16)
@@ -49,8 +49,10 @@
  * caller; the library keeps none after a call returns, allocates nothing,
  * and never synchronises the stream.  Calls are asynchronous on `stream`
  * (a cudaStream_t; NULL = the legacy default stream).  Active requests must
- * use distinct slots; two calls that touch the same slots or counters must
- * not run concurrently.  In replay mode the verify and the commit must see
+ * use distinct slots; two calls that touch the same slots or the same work
+ * buffer must not run concurrently.  Each call is two kernel launches (a
+ * prologue and the rows) chained with programmatic dependent launch; the
+ * prologue waits for whatever ran before it on the stream.  In replay mode the verify and the commit must see
  * the same x, g, beta, conv_w and slot contents.
  *
  * Errors.  Host return codes: GDN_OK, or GDN_ERR_* for arguments the host
@@ -68,6 +70,7 @@
 #ifndef GDNSPEC_H
 #define GDNSPEC_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -76,8 +79,6 @@ extern "C" {
 
 #define GDN_API __attribute__((visibility("default")))
 
-/* Length of `counters` per (request, q/k head). */
-#define GDN_COUNTERS_PER_QK_HEAD 8
 
 enum {
   GDN_OK = 0,
@@ -122,7 +123,7 @@ typedef struct gdn_args {
   float* o;                  /* verify and fused calls only                    */
   float* scratch_S;          /* snapshot mode only                             */
   void* scratch_cs;          /* snapshot mode only                             */
-  int32_t* counters;         /* replay commit and fused calls only             */
+  void* work;                /* verify, replay commit and fused calls          */
   int32_t* status;           /* may be NULL                                    */
 } gdn_args;
 
@@ -131,21 +132,27 @@ typedef struct gdn_args {
  * mode GDN_SNAPSHOT also writes, per row t, the state and conv window a
  * commit at accept_len = t would leave into scratch_S / scratch_cs[b][t]
  * (the widened verify state).  Needs: x, g, beta, conv_w, conv_state,
- * ssm_state, slot_ids, n_rows, o (+ scratch_S, scratch_cs in snapshot mode). */
+ * ssm_state, slot_ids, n_rows, work, o (+ scratch_S, scratch_cs in snapshot
+ * mode). */
 GDN_API int gdn_verify(const gdn_args* args, int mode, void* stream);
 
 /* Commit: make slot slot_ids[b] hold the state and conv window after rows
  * 0..accept_len[b] of request b.  mode GDN_REPLAY reruns those rows from the
  * committed state (same arithmetic as the verify, so the result equals a
- * fused call bit for bit) and needs the verify's inputs plus accept_len and
- * counters; mode GDN_SNAPSHOT copies row accept_len[b] of a snapshot verify's
+ * fused call bit for bit) and needs the verify's inputs plus accept_len;
+ * mode GDN_SNAPSHOT copies row accept_len[b] of a snapshot verify's
  * scratch and needs slot_ids, n_rows, accept_len, scratch_S, scratch_cs. */
 GDN_API int gdn_commit(const gdn_args* args, int mode, void* stream);
 
 /* Verify and commit in one pass over the state: writes o for every valid
  * row and, at row accept_len[b], the slot.  Each state byte is read once and
- * written once.  Needs everything gdn_verify needs plus accept_len, counters. */
+ * written once.  Needs everything gdn_verify needs plus accept_len. */
 GDN_API int gdn_verify_commit(const gdn_args* args, void* stream);
+
+/* Bytes of `work` a verify, replay commit or fused call with these shapes
+ * needs: 4 * B * R * (2 * H_qk * d_k + H_v * d_v + H_qk).  Reads only the
+ * size fields of args; 0 if they are invalid or unsupported. */
+GDN_API size_t gdn_work_bytes(const gdn_args* args);
 
 /* Static description of a return code (never NULL). */
 GDN_API const char* gdn_strerror(int code);

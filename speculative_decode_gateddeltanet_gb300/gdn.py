@@ -16,7 +16,6 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libgdnspec.so"
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH = 0, 1, 2, 3, 4
 STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT = 1, 2, 4
 BF16, F32 = 0, 1
-COUNTERS_PER_QK_HEAD = 8
 REPLAY, SNAPSHOT = 0, 1
 
 _I32, _F32, _P = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
@@ -31,7 +30,7 @@ class GdnArgs(ctypes.Structure):
         ("flags", _I32),
         ("x", _P), ("g", _P), ("beta", _P), ("conv_w", _P), ("conv_state", _P), ("ssm_state", _P),
         ("slot_ids", _P), ("n_rows", _P), ("accept_len", _P), ("o", _P), ("scratch_S", _P),
-        ("scratch_cs", _P), ("counters", _P), ("status", _P),
+        ("scratch_cs", _P), ("work", _P), ("status", _P),
     ]
 
 
@@ -50,12 +49,19 @@ _lib.gdn_commit.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int, _P]
 _lib.gdn_verify_commit.argtypes = [ctypes.POINTER(GdnArgs), _P]
 for _f in (_lib.gdn_verify, _lib.gdn_commit, _lib.gdn_verify_commit):
     _f.restype = ctypes.c_int
+_lib.gdn_work_bytes.argtypes = [ctypes.POINTER(GdnArgs)]
+_lib.gdn_work_bytes.restype = ctypes.c_size_t
 _lib.gdn_strerror.argtypes = [ctypes.c_int]
 _lib.gdn_strerror.restype = ctypes.c_char_p
 
 
 def strerror(code: int) -> str:
     return _lib.gdn_strerror(code).decode()
+
+
+def work_bytes(args: GdnArgs) -> int:
+    """Bytes of scratch a call with these shapes needs (0 if the shapes are invalid)."""
+    return int(_lib.gdn_work_bytes(ctypes.byref(args)))
 
 
 def _stream(stream) -> int | None:
@@ -88,7 +94,7 @@ def _ptr(t) -> int | None:
 
 
 def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_qk: int,
-              accept_len=None, o=None, scratch_S=None, scratch_cs=None, counters=None,
+              accept_len=None, o=None, scratch_S=None, scratch_cs=None, work=None,
               status=None, scale: float | None = None, l2_eps: float = 1e-6) -> GdnArgs:
     """Fill a GdnArgs from tensors laid out as ``include/gdnspec.h`` states.
 
@@ -109,7 +115,7 @@ def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_
         x=_ptr(x), g=_ptr(g), beta=_ptr(beta), conv_w=_ptr(conv_w), conv_state=_ptr(conv_state),
         ssm_state=_ptr(ssm_state), slot_ids=_ptr(slot_ids), n_rows=_ptr(n_rows),
         accept_len=_ptr(accept_len), o=_ptr(o), scratch_S=_ptr(scratch_S),
-        scratch_cs=_ptr(scratch_cs), counters=_ptr(counters), status=_ptr(status))
+        scratch_cs=_ptr(scratch_cs), work=_ptr(work), status=_ptr(status))
 
 
 class DeviceLayer:
@@ -117,7 +123,7 @@ class DeviceLayer:
 
     Built from a dict of CPU tensors (the layout ``inputs.make_layer`` uses).
     ``o`` is filled with NaN so rows a call must not write stay visibly
-    untouched; ``counters`` and ``status`` start at zero."""
+    untouched; ``status`` starts at zero; ``work`` is sized by the library."""
 
     KEYS = ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows", "accept_len")
 
@@ -128,18 +134,19 @@ class DeviceLayer:
         for k in self.KEYS:
             setattr(self, k, layer[k].to(device).contiguous())
         self.o = torch.full((s.B, s.R, s.H_v, s.d_v), float("nan"), device=device)
-        self.counters = torch.zeros(s.B * s.H_qk * COUNTERS_PER_QK_HEAD, dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.scratch_S = self.scratch_cs = None
         if snapshot:
             self.scratch_S = torch.empty((s.B, s.R, s.H_v, s.d_v, s.d_k), device=device)
             self.scratch_cs = torch.empty((s.B, s.R, s.C, s.W - 1), dtype=self.x.dtype, device=device)
         self.scale, self.l2_eps = scale, l2_eps
+        self.work = None
+        self.work = torch.empty(work_bytes(self.args()) // 4, dtype=torch.float32, device=device)
 
     def args(self) -> GdnArgs:
         return make_args(x=self.x, g=self.g, beta=self.beta, conv_w=self.conv_w,
                          conv_state=self.conv_state, ssm_state=self.ssm_state,
                          slot_ids=self.slot_ids, n_rows=self.n_rows, accept_len=self.accept_len,
                          o=self.o, scratch_S=self.scratch_S, scratch_cs=self.scratch_cs,
-                         counters=self.counters, status=self.status, H_qk=self.spec.H_qk,
+                         work=self.work, status=self.status, H_qk=self.spec.H_qk,
                          scale=self.scale, l2_eps=self.l2_eps)

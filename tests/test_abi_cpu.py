@@ -20,7 +20,8 @@ def declared_symbols():
 
 
 def test_header_declares_the_boundary():
-    assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_strerror"}
+    assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_work_bytes",
+                                      "gdn_strerror"}
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):
@@ -63,7 +64,7 @@ def good_args(gdn, **over):
     a = gdn.GdnArgs(B=2, R=4, H_qk=16, H_v=32, d_k=128, d_v=128, W=4, pool_slots=4,
                     in_dtype=gdn.BF16, scale=128 ** -0.5, l2_eps=1e-6, flags=0)
     for f in ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows",
-              "accept_len", "o", "scratch_S", "scratch_cs", "counters"):
+              "accept_len", "o", "scratch_S", "scratch_cs", "work"):
         setattr(a, f, FAKE)
     for k, v in over.items():
         setattr(a, k, v)
@@ -86,7 +87,8 @@ CASES = [
     ("null state", dict(ssm_state=None), 1),
     ("null o", dict(o=None), 1),
     ("null accept_len", dict(accept_len=None), 1),
-    ("null counters", dict(counters=None), 1),
+    ("null work", dict(work=None), 1),
+    ("misaligned work", dict(work=FAKE + 4), 3),
     ("misaligned state", dict(ssm_state=FAKE + 4), 3),
     ("misaligned o", dict(o=FAKE + 8), 3),
     ("misaligned x", dict(x=FAKE + 1), 3),
@@ -104,8 +106,8 @@ def test_fused_rejects_bad_arguments(cuda_lib, what, over, code):
 
 def test_mode_specific_requirements(cuda_lib):
     lib, g = cuda_lib._lib, cuda_lib
-    # verify needs no accept_len / counters; snapshot verify needs scratch
-    a = good_args(g, B=0, accept_len=None, counters=None)
+    # verify needs no accept_len; snapshot verify needs scratch
+    a = good_args(g, B=0, accept_len=None)
     assert lib.gdn_verify(ctypes.byref(a), g.REPLAY, None) == g.OK
     a = good_args(g, scratch_S=None)
     assert lib.gdn_verify(ctypes.byref(a), g.SNAPSHOT, None) == g.ERR_INVALID_ARG
@@ -115,8 +117,8 @@ def test_mode_specific_requirements(cuda_lib):
     assert lib.gdn_commit(ctypes.byref(a), g.SNAPSHOT, None) == g.ERR_INVALID_ARG
     a = good_args(g, B=0, x=None)
     assert lib.gdn_commit(ctypes.byref(a), g.SNAPSHOT, None) == g.OK
-    # replay commit needs counters
-    a = good_args(g, counters=None)
+    # replay commit needs the work buffer; snapshot commit does not
+    a = good_args(g, work=None)
     assert lib.gdn_commit(ctypes.byref(a), g.REPLAY, None) == g.ERR_INVALID_ARG
     assert lib.gdn_verify_commit(None, None) == g.ERR_INVALID_ARG
 
@@ -127,6 +129,14 @@ def test_empty_batch_is_a_no_op(cuda_lib):
                  lambda: cuda_lib._lib.gdn_verify(ctypes.byref(a), 0, None),
                  lambda: cuda_lib._lib.gdn_commit(ctypes.byref(a), 0, None)):
         assert call() == cuda_lib.OK
+
+
+def test_work_bytes(cuda_lib):
+    a = good_args(cuda_lib)
+    B, R, Hq, Hv, dk, dv = 2, 4, 16, 32, 128, 128
+    assert cuda_lib.work_bytes(a) == 4 * B * R * (2 * Hq * dk + Hv * dv + Hq)
+    assert cuda_lib.work_bytes(good_args(cuda_lib, d_k=96)) == 0
+    assert cuda_lib._lib.gdn_work_bytes(None) == 0
 
 
 def test_binding_raises_on_error(cuda_lib):

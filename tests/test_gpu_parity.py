@@ -155,7 +155,7 @@ def test_chained_single_rows_equal_one_call():
         a = gdn.make_args(x=x_t, g=g_t, beta=beta_t, conv_w=chain.conv_w,
                           conv_state=chain.conv_state, ssm_state=chain.ssm_state,
                           slot_ids=chain.slot_ids, n_rows=n_t, accept_len=torch.zeros_like(n_t),
-                          o=o_t, counters=chain.counters, status=chain.status, H_qk=spec.H_qk)
+                          o=o_t, work=chain.work, status=chain.status, H_qk=spec.H_qk)
         gdn.gdn_verify_commit(a)
         torch.cuda.synchronize()
         for b in range(spec.B):
@@ -208,7 +208,6 @@ def test_inactive_and_bad_requests_flagged_and_skipped():
         dev = run_gpu(layer, mode)
         assert int(dev.status.item()) == want, mode
         check_against_oracle(layer, dev, ref, commit=mode != "verify")
-        assert int(dev.counters.abs().sum().item()) == 0
     # all requests inactive: nothing written at all
     layer["n_rows"] = torch.zeros(6, dtype=torch.int32)
     dev = run_gpu(layer, "fused")
@@ -216,10 +215,9 @@ def test_inactive_and_bad_requests_flagged_and_skipped():
     assert torch.equal(bits(dev.ssm_state), bits(layer["ssm_state"]))
 
 
-def test_counters_left_zero_and_calls_repeat():
-    """Three fused calls in a row on the same buffers: the arrival counters
-    end at zero after each, and the third call's state equals the oracle run
-    three times."""
+def test_calls_repeat_on_the_same_buffers():
+    """Three fused calls in a row on the same buffers (state, windows and work
+    reused): the third call's state equals the oracle run three times."""
     from speculative_decode_gateddeltanet_gb300 import gdn
 
     (spec, seed), = workload_layers(SWEEP, batch=16)
@@ -229,7 +227,6 @@ def test_counters_left_zero_and_calls_repeat():
     for _ in range(3):
         gdn.gdn_verify_commit(dev.args())
         torch.cuda.synchronize()
-        assert int(dev.counters.abs().sum().item()) == 0
         r = oracle.verify_commit(cur)
         cur = dict(cur, ssm_state=torch.from_numpy(r["ssm_state"]).float(),
                    conv_state=torch.from_numpy(r["conv_state"]).to(torch.bfloat16))
@@ -257,7 +254,7 @@ def test_guard_bands_untouched():
     S.copy_(dev.ssm_state)
     a = gdn.make_args(x=dev.x, g=dev.g, beta=dev.beta, conv_w=dev.conv_w, conv_state=dev.conv_state,
                       ssm_state=S, slot_ids=dev.slot_ids, n_rows=dev.n_rows, accept_len=dev.accept_len,
-                      o=o, counters=dev.counters, status=dev.status, H_qk=spec.H_qk)
+                      o=o, work=dev.work, status=dev.status, H_qk=spec.H_qk)
     gdn.gdn_verify_commit(a)
     torch.cuda.synchronize()
     assert bool((o_buf[:G] == -7.0).all()) and bool((o_buf[-G:] == -7.0).all())
