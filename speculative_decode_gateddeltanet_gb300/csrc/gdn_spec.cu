@@ -75,9 +75,10 @@ struct Params {
   float* o;
   float* snapS;
   void* snapCs;
-  float* wqk;  // work: [B][R][H_qk][2][d_k]  scale*q^ | k^
-  float* wv;   // work: [B][R][H_v*d_v]       v
-  float* wkq;  // work: [B][R][H_qk]          k^ . (scale q^)
+  int dvs;     // state rows per rows-kernel item
+  float* wqk;  // work: [B][H_qk][R][2 d_k]         scale*q^ | k^
+  float* wv;   // work: [B][H_v d_v / dvs][R][dvs]  v
+  float* wsc;  // work: [B][H_v][R][4]              exp(g), beta, k^.(scale q^), 0
   int* status;
 };
 
@@ -192,6 +193,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -247,7 +251,10 @@ __device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, i
 
 // ------------------------------------------------------------ prologue
 // grid (H_qk + ceil(H_v d_v / 256), B): block x < H_qk holds the 2 d_k q and k
-// channels of q/k head x, the other blocks 256 v channels each.
+// channels of q/k head x, the other blocks 256 v channels each.  Work layout:
+//   wqk [B][H_qk][R][2 d_k]   scale*q^ | k^       (one contiguous run per (b, q/k head))
+//   wv  [B][H_v d_v/DVS][R][DVS]  v               (one run per (b, head, row slice))
+//   wsc [B][H_v][R][4]        exp(g), beta, k^.(scale q^), 0   (one run per (b, head))
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
@@ -283,33 +290,45 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     const T* xg = static_cast<const T*>(p.x) + (size_t)b * p.R * p.C + ch;
     const T* wg = static_cast<const T*>(p.conv_w) + ch * kW;
     T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
-    const float w0 = tof(wg[0]), w1 = tof(wg[1]), w2 = tof(wg[2]), w3 = tof(wg[3]);
+    // every load first, so they are all in flight together
+    T xr[kMaxR];
+#pragma unroll
+    for (int t = 0; t < kMaxR; ++t)
+      if (t < t_end) xr[t] = xg[(size_t)t * p.C];
+    const T q0 = wg[0], q1 = wg[1], q2 = wg[2], q3 = wg[3];
     T r0 = cs[0], r1 = cs[1], r2 = cs[2];  // window, oldest first, kept as stored
-    T c0 = r0, c1 = r1, c2 = r2;           // window after row a
-    for (int t = 0; t < t_end; ++t) {
-      const T r3 = xg[(size_t)t * p.C];
-      float z = __fmul_rn(w0, tof(r0));
-      z = __fmaf_rn(w1, tof(r1), z);
-      z = __fmaf_rn(w2, tof(r2), z);
-      z = __fmaf_rn(w3, tof(r3), z);
-      const float y = silu(z);
-      if (qk_block)
-        sy[t][tid] = y;
-      else
-        p.wv[((size_t)b * p.R + t) * p.H_v * p.d_v + vi] = y;
-      r0 = r1;
-      r1 = r2;
-      r2 = r3;
-      if (kSnap) {
-        T* sc = static_cast<T*>(p.snapCs) + (((size_t)b * p.R + t) * p.C + ch) * kWS;
-        sc[0] = r0;
-        sc[1] = r1;
-        sc[2] = r2;
-      }
-      if (kCommits && t == a) {
-        c0 = r0;
-        c1 = r1;
-        c2 = r2;
+    const float w0 = tof(q0), w1 = tof(q1), w2 = tof(q2), w3 = tof(q3);
+    T c0 = r0, c1 = r1, c2 = r2;  // window after row a
+    float* vdst = nullptr;
+    if (!qk_block)
+      vdst = p.wv + (((size_t)b * p.H_v * p.slices + vi / p.dvs) * p.R) * p.dvs + (vi % p.dvs);
+#pragma unroll
+    for (int t = 0; t < kMaxR; ++t) {
+      if (t < t_end) {
+        const T r3 = xr[t];
+        float z = __fmul_rn(w0, tof(r0));
+        z = __fmaf_rn(w1, tof(r1), z);
+        z = __fmaf_rn(w2, tof(r2), z);
+        z = __fmaf_rn(w3, tof(r3), z);
+        const float y = silu(z);
+        if (qk_block)
+          sy[t][tid] = y;
+        else
+          vdst[(size_t)t * p.dvs] = y;
+        r0 = r1;
+        r1 = r2;
+        r2 = r3;
+        if (kSnap) {
+          T* sc = static_cast<T*>(p.snapCs) + (((size_t)b * p.R + t) * p.C + ch) * kWS;
+          sc[0] = r0;
+          sc[1] = r1;
+          sc[2] = r2;
+        }
+        if (kCommits && t == a) {
+          c0 = r0;
+          c1 = r1;
+          c2 = r2;
+        }
       }
     }
     if (kCommits && commit) {  // this thread was the channel's only reader in the call
@@ -345,13 +364,29 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   }
   __syncthreads();
   if (active) {
-    for (int t = 0; t < t_end; ++t)
-      p.wqk[(((size_t)b * p.R + t) * p.H_qk + hq) * 2 * DK + tid] = __fmul_rn(sy[t][tid], sf[t][tid < DK ? 0 : 1]);
+    float* dst = p.wqk + ((size_t)b * p.H_qk + hq) * p.R * 2 * DK + tid;
+    for (int t = 0; t < t_end; ++t) dst[(size_t)t * 2 * DK] = __fmul_rn(sy[t][tid], sf[t][tid < DK ? 0 : 1]);
   }
-  if (tid < t_end) p.wkq[((size_t)b * p.R + tid) * p.H_qk + hq] = sf[tid][2];
+  // per-row scalars of the value heads that read this q/k head
+  for (int i = tid; i < p.G * t_end; i += kPrepThreads) {
+    const int h = hq * p.G + i / t_end, t = i % t_end;
+    const size_t gi = ((size_t)b * p.R + t) * p.H_v + h;
+    *reinterpret_cast<float4*>(p.wsc + (((size_t)b * p.H_v + h) * p.R + t) * 4) =
+        make_float4(expf(__ldg(p.g + gi)), __ldg(p.beta + gi), sf[t][2], 0.f);
+  }
 }
 
 // ------------------------------------------------------------ the rows
+// Persistent: CTA j runs items j, j + gridDim.x, ...; item = (request b,
+// value head h, row slice sl), numbered ((b H_v) + h) slices + sl.  Two
+// shared-memory stages: while one item computes, the next one's state slice
+// (one bulk copy), q/k rows, v rows and per-row scalars are in flight.
+template <int DK>
+struct Stage {
+  static constexpr int DVS = Geo<DK>::DVS;
+  __host__ __device__ static int floats(int R) { return DVS * DK + R * 2 * DK + R * DVS + R * 4; }
+};
+
 template <int DK, int MODE>
 __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(const Params p) {
   using Gm = Geo<DK>;
@@ -362,150 +397,214 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   constexpr bool kSnap = MODE == kVerifySnap;
   constexpr int V = kWantO ? 2 * M : M;
   constexpr int kDupMask = (LPR >> ilog2(V)) - 1;  // lanes that repeat a finished sum
+  constexpr uint32_t kSBytes = DVS * DK * sizeof(float);
 
-  const int b = blockIdx.y;
-  const int h = blockIdx.x / p.slices;
-  const int sl = blockIdx.x - h * p.slices;
-  const int hq = h / p.G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_items = p.B * p.H_v * p.slices;
+  const int R = p.R;
+  const int sfl = Stage<DK>::floats(R);
+  extern __shared__ __align__(16) float smem[];
+  __shared__ __align__(8) uint64_t barS[2], barQ[2];
+  __shared__ int sMeta[2][3];  // per stage: slot, rows to run, commit row (-1 none)
 
-  int slot, a, report;
-  bool commit;
-  const int t_end = request_rows<kCommits, MODE == kCommitReplay>(p, b, slot, a, commit, report);
-  if (report && h == 0 && sl == 0 && tid == 0) flag(p.status, report);
-  if (t_end == 0) return;
+  auto stS = [&](int s) { return smem + (size_t)s * sfl; };
+  auto stQK = [&](int s) { return stS(s) + DVS * DK; };
+  auto stV = [&](int s) { return stQK(s) + R * 2 * DK; };
+  auto stSC = [&](int s) { return stV(s) + R * DVS; };
 
-  // ---- state slice -> registers (before the prologue is waited for) ----
+  // ---- producer side (thread 0) ----
+  auto meta = [&](int it, int& slot, int& rows, int& commit_row) {
+    const int b = it / (p.H_v * p.slices);
+    const int hs = it - b * p.H_v * p.slices;
+    int a, report;
+    bool commit;
+    rows = request_rows<kCommits, MODE == kCommitReplay>(p, b, slot, a, commit, report);
+    if (report && hs == 0) flag(p.status, report);
+    commit_row = commit ? a : -1;
+  };
+  auto issue_state = [&](int s, int it, int slot) {
+    const int b = it / (p.H_v * p.slices);
+    const int hs = it - b * p.H_v * p.slices;  // h * slices + sl
+    mbar_expect_tx(&barS[s], kSBytes);
+    bulk_load(stS(s), p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS[s]);
+  };
+  auto issue_rows = [&](int s, int it, int rows) {
+    const int b = it / (p.H_v * p.slices);
+    const int hs = it - b * p.H_v * p.slices;
+    const int h = hs / p.slices;
+    const int hq = h / p.G;
+    mbar_expect_tx(&barQ[s], (uint32_t)(rows * (2 * DK + DVS + 4) * sizeof(float)));
+    bulk_load(stQK(s), p.wqk + ((size_t)b * p.H_qk + hq) * R * 2 * DK, rows * 2 * DK * sizeof(float), &barQ[s]);
+    bulk_load(stV(s), p.wv + ((size_t)b * p.H_v * p.slices + hs) * R * DVS, rows * DVS * sizeof(float), &barQ[s]);
+    bulk_load(stSC(s), p.wsc + ((size_t)b * p.H_v + h) * R * 4, rows * 4 * sizeof(float), &barQ[s]);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&barS[s], 1);
+      mbar_init(&barQ[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {  // state slices of the first two items: before the prologue ends
+      const int it = blockIdx.x + s * gridDim.x;
+      int slot = 0, rows = 0, crow = -1;
+      if (it < n_items) meta(it, slot, rows, crow);
+      sMeta[s][0] = slot;
+      sMeta[s][1] = rows;
+      sMeta[s][2] = crow;
+      if (rows > 0)
+        issue_state(s, it, slot);
+      else
+        mbar_arrive(&barS[s]);
+    }
+  }
+  pdl_wait();  // the prologue's q, k, v and scalars are complete and visible
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      const int it = blockIdx.x + s * gridDim.x;
+      if (sMeta[s][1] > 0)
+        issue_rows(s, it, sMeta[s][1]);
+      else
+        mbar_arrive(&barQ[s]);
+    }
+  }
+  __syncthreads();
+
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
   const int wrow = warp * ROWS_W + rg;  // slice-local row of m = 0; row m adds m * RG
-  const size_t head_elems = (size_t)p.d_v * DK;
-  float* Sg = p.S + ((size_t)slot * p.H_v + h) * head_elems + (size_t)sl * DVS * DK;
-  f2 S[M][2 * NC4];  // column pairs of the lane's 4-column chunks
-#pragma unroll
-  for (int m = 0; m < M; ++m)
-#pragma unroll
-    for (int j = 0; j < NC4; ++j) {
-      const ulonglong2 v =
-          *reinterpret_cast<const ulonglong2*>(Sg + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j));
-      S[m][2 * j] = v.x;
-      S[m][2 * j + 1] = v.y;
-    }
-
-  // ---- shared memory: [R][2 DK] scale*q^ | k^,  [R][DVS] v,  per-row scalars ----
-  extern __shared__ __align__(16) float smem[];
-  float* sQK = smem;
-  float* sV = sQK + (size_t)p.R * 2 * DK;
-  float* sA = sV + (size_t)p.R * DVS;
-  float* sBt = sA + kMaxR;
-  float* sKQ = sBt + kMaxR;
-  __shared__ __align__(8) uint64_t bar;
-  if (tid == 0) mbar_init(&bar, 1);
-  __syncthreads();
-
-  pdl_wait();  // the prologue's q, k, v are complete and visible
-  if (warp == 0) {
-    if (lane == 0) mbar_expect_tx(&bar, (uint32_t)(t_end * (2 * DK + DVS) * sizeof(float)));
-    __syncwarp();
-    for (int i = lane; i < 2 * t_end; i += 32) {
-      if (i < t_end)
-        bulk_load(sQK + i * 2 * DK, p.wqk + (((size_t)b * p.R + i) * p.H_qk + hq) * 2 * DK,
-                  2 * DK * sizeof(float), &bar);
-      else
-        bulk_load(sV + (i - t_end) * DVS,
-                  p.wv + ((size_t)b * p.R + (i - t_end)) * p.H_v * p.d_v + (size_t)h * p.d_v + (size_t)sl * DVS,
-                  DVS * sizeof(float), &bar);
-    }
-  }
-  if (tid < t_end) {
-    const size_t gi = ((size_t)b * p.R + tid) * p.H_v + h;
-    sA[tid] = expf(__ldg(p.g + gi));
-    sBt[tid] = __ldg(p.beta + gi);
-    sKQ[tid] = p.wkq[((size_t)b * p.R + tid) * p.H_qk + hq];
-  }
-  const bool late = !mbar_wait(&bar, 0);
-  if (__syncthreads_or(late)) {
-    if (tid == 0) flag(p.status, GDN_STATUS_TIMEOUT);
-    mbar_wait(&bar, 0);  // bounded: let copies still in flight land before leaving
-    return;
-  }
-
-  // ---- the rows ----
-  float* og = nullptr;
-  if (kWantO) og = p.o + ((size_t)b * p.R * p.H_v + h) * p.d_v + (size_t)sl * DVS;
-  const size_t o_tstride = (size_t)p.H_v * p.d_v;
   const int gbase = lane & ~(LPR - 1);
-  for (int t = 0; t < t_end; ++t) {
-    const float alpha = sA[t], bt = sBt[t];
-    const f2 alpha2 = pack2(alpha, alpha);
-    const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + DK);
-    f2 kv[2 * NC4];
-#pragma unroll
-    for (int j = 0; j < NC4; ++j) {
-      const ulonglong2 v = k4[c + LPR * j];
-      kv[2 * j] = v.x;
-      kv[2 * j + 1] = v.y;
-    }
-    float part_v[V];
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      f2 acc = fma2(S[m][0], kv[0], pack2(0.f, 0.f));
-#pragma unroll
-      for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], kv[j], acc);
-      part_v[m] = sum2(acc);
-    }
-    if constexpr (kWantO) {
-      const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK);
-      f2 qv[2 * NC4];
-#pragma unroll
-      for (int j = 0; j < NC4; ++j) {
-        const ulonglong2 v = q4[c + LPR * j];
-        qv[2 * j] = v.x;
-        qv[2 * j + 1] = v.y;
-      }
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        f2 acc = fma2(S[m][0], qv[0], pack2(0.f, 0.f));
-#pragma unroll
-        for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], qv[j], acc);
-        part_v[(M + m) % V] = sum2(acc);
-      }
-    }
-    int idx;
-    const float red = reduce_scatter<LPR, V>(part_v, lane, idx);
-    const int mrow = idx % M;
-    const int rloc = wrow + mrow * RG;
-    // u is meaningful on the lanes holding an S k sum (idx < M)
-    const float u = __fmul_rn(bt, __fsub_rn(sV[t * DVS + rloc], __fmul_rn(alpha, red)));
-    if constexpr (kWantO) {
-      const float up = __shfl_xor_sync(kFull, u, LPR / 2);  // u of the same row
-      if (idx >= M && (c & kDupMask) == 0)
-        og[(size_t)t * o_tstride + rloc] = __fmaf_rn(up, sKQ[t], __fmul_rn(alpha, red));
-    }
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      const float um = __shfl_sync(kFull, u, gbase | value_lane<LPR, V>(m));
-      const f2 u2 = pack2(um, um);
-#pragma unroll
-      for (int j = 0; j < 2 * NC4; ++j) S[m][j] = fma2(u2, kv[j], mul2(alpha2, S[m][j]));
+  const size_t o_tstride = (size_t)p.H_v * p.d_v;
+
+  for (int k = 0;; ++k) {
+    const int it = blockIdx.x + k * gridDim.x;
+    if (it >= n_items) break;
+    const int s = k & 1;
+    const uint32_t ph = (k >> 1) & 1;
+    const int slot = sMeta[s][0], rows = sMeta[s][1], a = sMeta[s][2];
+    // producer: meta of the item two ahead, in flight while this one runs
+    const int it2 = it + 2 * gridDim.x;
+    int slot2 = 0, rows2 = 0, crow2 = -1;
+    if (tid == 0 && it2 < n_items) meta(it2, slot2, rows2, crow2);
+
+    const bool late = !(mbar_wait(&barS[s], ph) && mbar_wait(&barQ[s], ph));
+    if (__syncthreads_or(late)) {
+      if (tid == 0) flag(p.status, GDN_STATUS_TIMEOUT);
+      mbar_wait(&barS[s], ph);  // bounded: let copies still in flight land before leaving
+      mbar_wait(&barQ[s], ph);
+      mbar_wait(&barS[s ^ 1], ph ^ (s ? 1u : 0u));
+      mbar_wait(&barQ[s ^ 1], ph ^ (s ? 1u : 0u));
+      return;
     }
 
-    if (kCommits && commit && t == a) {
+    if (rows > 0) {
+      const int b = it / (p.H_v * p.slices);
+      const int hs = it - b * p.H_v * p.slices;
+      const int h = hs / p.slices, sl = hs - h * p.slices;
+      // ---- state slice: shared memory -> registers ----
+      const float* sS = stS(s);
+      f2 S[M][2 * NC4];  // column pairs of the lane's 4-column chunks
 #pragma unroll
       for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int j = 0; j < NC4; ++j)
-          *reinterpret_cast<ulonglong2*>(Sg + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
-              make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+        for (int j = 0; j < NC4; ++j) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(sS + (wrow + m * RG) * DK + 4 * (c + LPR * j));
+          S[m][2 * j] = v.x;
+          S[m][2 * j + 1] = v.y;
+        }
+      const float* sQK = stQK(s);
+      const float* sV = stV(s);
+      const float* sSC = stSC(s);
+      float* Sg = p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK;
+      float* og = nullptr;
+      if (kWantO) og = p.o + ((size_t)b * R * p.H_v + h) * p.d_v + (size_t)sl * DVS;
+
+      for (int t = 0; t < rows; ++t) {
+        const float4 sc = *reinterpret_cast<const float4*>(sSC + 4 * t);  // alpha, beta, k.q
+        const float alpha = sc.x, bt = sc.y;
+        const f2 alpha2 = pack2(alpha, alpha);
+        const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + DK);
+        f2 kv[2 * NC4];
+#pragma unroll
+        for (int j = 0; j < NC4; ++j) {
+          const ulonglong2 v = k4[c + LPR * j];
+          kv[2 * j] = v.x;
+          kv[2 * j + 1] = v.y;
+        }
+        float part_v[V];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          f2 acc = fma2(S[m][0], kv[0], pack2(0.f, 0.f));
+#pragma unroll
+          for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], kv[j], acc);
+          part_v[m] = sum2(acc);
+        }
+        if constexpr (kWantO) {
+          const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK);
+          f2 qv[2 * NC4];
+#pragma unroll
+          for (int j = 0; j < NC4; ++j) {
+            const ulonglong2 v = q4[c + LPR * j];
+            qv[2 * j] = v.x;
+            qv[2 * j + 1] = v.y;
+          }
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            f2 acc = fma2(S[m][0], qv[0], pack2(0.f, 0.f));
+#pragma unroll
+            for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], qv[j], acc);
+            part_v[(M + m) % V] = sum2(acc);
+          }
+        }
+        int idx;
+        const float red = reduce_scatter<LPR, V>(part_v, lane, idx);
+        const int mrow = idx % M;
+        const int rloc = wrow + mrow * RG;
+        // u is meaningful on the lanes holding an S k sum (idx < M)
+        const float u = __fmul_rn(bt, __fsub_rn(sV[t * DVS + rloc], __fmul_rn(alpha, red)));
+        if constexpr (kWantO) {
+          const float up = __shfl_xor_sync(kFull, u, LPR / 2);  // u of the same row
+          if (idx >= M && (c & kDupMask) == 0)
+            og[(size_t)t * o_tstride + rloc] = __fmaf_rn(up, sc.z, __fmul_rn(alpha, red));
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float um = __shfl_sync(kFull, u, gbase | value_lane<LPR, V>(m));
+          const f2 u2 = pack2(um, um);
+#pragma unroll
+          for (int j = 0; j < 2 * NC4; ++j) S[m][j] = fma2(u2, kv[j], mul2(alpha2, S[m][j]));
+        }
+
+        if (kCommits && t == a) {
+#pragma unroll
+          for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int j = 0; j < NC4; ++j)
+              *reinterpret_cast<ulonglong2*>(Sg + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
+                  make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+        }
+        if (kSnap) {
+          float* Ss = p.snapS + (((size_t)b * R + t) * p.H_v * p.slices + hs) * DVS * DK;
+#pragma unroll
+          for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int j = 0; j < NC4; ++j)
+              *reinterpret_cast<ulonglong2*>(Ss + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
+                  make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+        }
+      }
     }
-    if (kSnap) {
-      float* Ss = p.snapS + (((size_t)b * p.R + t) * p.H_v + h) * head_elems + (size_t)sl * DVS * DK;
-#pragma unroll
-      for (int m = 0; m < M; ++m)
-#pragma unroll
-        for (int j = 0; j < NC4; ++j)
-          *reinterpret_cast<ulonglong2*>(Ss + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
-              make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+    __syncthreads();  // stage s is consumed: refill it with the item two ahead
+    if (tid == 0 && it2 < n_items) {
+      sMeta[s][0] = slot2;
+      sMeta[s][1] = rows2;
+      sMeta[s][2] = crow2;
+      if (rows2 > 0) {
+        issue_state(s, it2, slot2);
+        issue_rows(s, it2, rows2);
+      } else {
+        mbar_arrive(&barS[s]);
+        mbar_arrive(&barQ[s]);
+      }
     }
   }
   pdl_trigger();  // the next call's prologue may launch once every CTA is here
@@ -551,11 +650,37 @@ int launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, c
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
+// Persistent grid of the rows kernel: as many CTAs as fit at once, trimmed so
+// every CTA runs the same number of items.
 template <int DK, int MODE>
 int launch_rows(const Params& p, cudaStream_t st) {
   using Gm = Geo<DK>;
-  const size_t smem = sizeof(float) * ((size_t)p.R * (2 * DK + Gm::DVS) + 3 * kMaxR);
-  return launch(rows_kernel<DK, MODE>, dim3(p.H_v * p.slices, p.B), dim3(Gm::NT), smem, st, p);
+  const size_t smem = 2 * sizeof(float) * (size_t)Stage<DK>::floats(p.R);
+  struct Cache {
+    int dev = -1;
+    size_t smem = 0;
+    int ctas = 0;  // resident CTAs on the device for this shared-memory size
+  };
+  static Cache cache;  // per instantiation
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (cache.dev != dev || cache.smem != smem) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(rows_kernel<DK, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+      return GDN_ERR_LAUNCH;
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rows_kernel<DK, MODE>, Gm::NT, smem) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per_sm < 1)
+      return GDN_ERR_LAUNCH;
+    cache.dev = dev;
+    cache.smem = smem;
+    cache.ctas = per_sm * sms;
+  }
+  const long long items = (long long)p.B * p.H_v * p.slices;
+  const long long per_cta = (items + cache.ctas - 1) / cache.ctas;
+  const int grid = (int)((items + per_cta - 1) / per_cta);
+  return launch(rows_kernel<DK, MODE>, dim3(grid), dim3(Gm::NT), smem, st, p);
 }
 
 template <int MODE>
@@ -609,13 +734,14 @@ int check_shape(const gdn_args* a) {
   return GDN_OK;
 }
 
-size_t work_floats(const gdn_args* a, size_t* off_v, size_t* off_kq) {
+// Work buffer: wqk [B][H_qk][R][2 d_k], wv [B][R-major v rows per slice], wsc [B][H_v][R][4].
+size_t work_floats(const gdn_args* a, size_t* off_v, size_t* off_sc) {
   const size_t rows = (size_t)a->B * a->R;
   const size_t qk = rows * a->H_qk * 2 * a->d_k;
   const size_t v = rows * a->H_v * a->d_v;
   if (off_v) *off_v = qk;
-  if (off_kq) *off_kq = qk + v;
-  return qk + v + rows * a->H_qk;
+  if (off_sc) *off_sc = qk + v;
+  return qk + v + rows * a->H_v * 4;
 }
 
 int validate(const gdn_args* a, unsigned need, Params* out) {
@@ -672,11 +798,12 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.o = a->o;
   p.snapS = a->scratch_S;
   p.snapCs = a->scratch_cs;
-  size_t off_v = 0, off_kq = 0;
-  work_floats(a, &off_v, &off_kq);
+  p.dvs = rows_per_cta(a->d_k);
+  size_t off_v = 0, off_sc = 0;
+  work_floats(a, &off_v, &off_sc);
   p.wqk = static_cast<float*>(a->work);
   p.wv = p.wqk ? p.wqk + off_v : nullptr;
-  p.wkq = p.wqk ? p.wqk + off_kq : nullptr;
+  p.wsc = p.wqk ? p.wqk + off_sc : nullptr;
   p.status = a->status;
   return GDN_OK;
 }
