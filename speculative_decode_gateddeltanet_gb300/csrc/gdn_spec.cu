@@ -88,12 +88,12 @@ struct Geo {
   static constexpr int LPR = DK >= 32 ? 8 : 4;   // lanes per state row
   static constexpr int NC4 = DK / (4 * LPR);     // 4-column chunks per lane per row
   static constexpr int RG = 32 / LPR;            // row groups per warp
-  static constexpr int M = 2;                    // rows per lane
+  static constexpr int M = DK >= 64 ? 4 : 2;     // rows per lane
   static constexpr int ROWS_W = RG * M;          // rows per warp
-  static constexpr int NW = DK >= 32 ? 4 : 1;    // warps per CTA
-  static constexpr int DVS = NW * ROWS_W;        // state rows per CTA
+  static constexpr int NW = DK == 16 ? 1 : (M == 4 ? 2 : 4);  // warps per CTA
+  static constexpr int DVS = NW * ROWS_W;        // state rows per CTA (32, or 16 at d_k = 16)
   static constexpr int NT = NW * 32;
-  static constexpr int MIN_CTAS = DK >= 32 ? 5 : 16;  // resident CTAs per SM the registers must allow
+  static constexpr int MIN_CTAS = NT == 64 ? 8 : (NT == 128 ? 5 : 16);  // resident CTAs per SM the registers must allow
 };
 
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
@@ -286,6 +286,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     ch = 2LL * p.H_qk * DK + vi;
   }
 
+  // gating of the value heads that read this q/k head: loaded now, written at the end
+  float g_i = 0.f, beta_i = 0.f;
+  if (qk_block && tid < p.G * t_end) {
+    const size_t gi = ((size_t)b * p.R + tid % t_end) * p.H_v + hq * p.G + tid / t_end;
+    g_i = __ldg(p.g + gi);
+    beta_i = __ldg(p.beta + gi);
+  }
   if (active) {
     const T* xg = static_cast<const T*>(p.x) + (size_t)b * p.R * p.C + ch;
     const T* wg = static_cast<const T*>(p.conv_w) + ch * kW;
@@ -370,9 +377,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   // per-row scalars of the value heads that read this q/k head
   for (int i = tid; i < p.G * t_end; i += kPrepThreads) {
     const int h = hq * p.G + i / t_end, t = i % t_end;
-    const size_t gi = ((size_t)b * p.R + t) * p.H_v + h;
+    if (i >= kPrepThreads) {  // more (head, row) pairs than threads: load now
+      const size_t gi = ((size_t)b * p.R + t) * p.H_v + h;
+      g_i = __ldg(p.g + gi);
+      beta_i = __ldg(p.beta + gi);
+    }
     *reinterpret_cast<float4*>(p.wsc + (((size_t)b * p.H_v + h) * p.R + t) * 4) =
-        make_float4(expf(__ldg(p.g + gi)), __ldg(p.beta + gi), sf[t][2], 0.f);
+        make_float4(expf(g_i), beta_i, sf[t][2], 0.f);
   }
 }
 
