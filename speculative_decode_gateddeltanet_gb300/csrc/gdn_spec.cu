@@ -193,6 +193,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
 }
+// Orders this CTA's earlier generic-proxy shared-memory accesses before later
+// bulk async copies (the async proxy) into the same memory.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -389,13 +392,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
 
 // ------------------------------------------------------------ the rows
 // Persistent: CTA j runs items j, j + gridDim.x, ...; item = (request b,
-// value head h, row slice sl), numbered ((b H_v) + h) slices + sl.  Two
-// shared-memory stages: while one item computes, the next one's state slice
-// (one bulk copy), q/k rows, v rows and per-row scalars are in flight.
+// value head h, row slice sl), numbered ((b H_v) + h) slices + sl.  The state
+// slice has one shared-memory buffer: as soon as an item's slice is in
+// registers, the next item's slice (one bulk copy) is requested, so it is in
+// flight while the item computes.  The item's q/k rows, v rows and per-row
+// scalars are small and double-buffered.
 template <int DK>
 struct Stage {
   static constexpr int DVS = Geo<DK>::DVS;
-  __host__ __device__ static int floats(int R) { return DVS * DK + R * 2 * DK + R * DVS + R * 4; }
+  __host__ __device__ static int rows_floats(int R) { return R * 2 * DK + R * DVS + R * 4; }
+  __host__ __device__ static size_t bytes(int R) { return sizeof(float) * ((size_t)DVS * DK + 2 * (size_t)rows_floats(R)); }
 };
 
 template <int DK, int MODE>
@@ -413,15 +419,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_items = p.B * p.H_v * p.slices;
   const int R = p.R;
-  const int sfl = Stage<DK>::floats(R);
+  const int rfl = Stage<DK>::rows_floats(R);
   extern __shared__ __align__(16) float smem[];
-  __shared__ __align__(8) uint64_t barS[2], barQ[2];
-  __shared__ int sMeta[2][3];  // per stage: slot, rows to run, commit row (-1 none)
-
-  auto stS = [&](int s) { return smem + (size_t)s * sfl; };
-  auto stQK = [&](int s) { return stS(s) + DVS * DK; };
-  auto stV = [&](int s) { return stQK(s) + R * 2 * DK; };
-  auto stSC = [&](int s) { return stV(s) + R * DVS; };
+  float* const stS = smem;  // [DVS][DK] state slice of the next item
+  auto stQK = [&](int s) { return smem + DVS * DK + (size_t)s * rfl; };  // [R][2 DK]
+  auto stV = [&](int s) { return stQK(s) + R * 2 * DK; };               // [R][DVS]
+  auto stSC = [&](int s) { return stV(s) + R * DVS; };                  // [R][4]
+  __shared__ __align__(8) uint64_t barS, barQ[2];
+  __shared__ int sMeta[2][3];  // per item parity: slot, rows to run, commit row (-1 none)
 
   // ---- producer side (thread 0) ----
   auto meta = [&](int it, int& slot, int& rows, int& commit_row) {
@@ -433,13 +438,21 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     if (report && hs == 0) flag(p.status, report);
     commit_row = commit ? a : -1;
   };
-  auto issue_state = [&](int s, int it, int slot) {
+  auto issue_state = [&](int it, int slot, int rows) {
+    if (rows == 0) {
+      mbar_arrive(&barS);
+      return;
+    }
     const int b = it / (p.H_v * p.slices);
     const int hs = it - b * p.H_v * p.slices;  // h * slices + sl
-    mbar_expect_tx(&barS[s], kSBytes);
-    bulk_load(stS(s), p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS[s]);
+    mbar_expect_tx(&barS, kSBytes);
+    bulk_load(stS, p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS);
   };
   auto issue_rows = [&](int s, int it, int rows) {
+    if (rows == 0) {
+      mbar_arrive(&barQ[s]);
+      return;
+    }
     const int b = it / (p.H_v * p.slices);
     const int hs = it - b * p.H_v * p.slices;
     const int h = hs / p.slices;
@@ -450,35 +463,24 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     bulk_load(stSC(s), p.wsc + ((size_t)b * p.H_v + h) * R * 4, rows * 4 * sizeof(float), &barQ[s]);
   };
 
+  int nslot = 0, nrows = 0, ncrow = -1;  // producer: meta of the item after the current one
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&barS[s], 1);
-      mbar_init(&barQ[s], 1);
+    mbar_init(&barS, 1);
+    mbar_init(&barQ[0], 1);
+    mbar_init(&barQ[1], 1);
+    if (blockIdx.x < n_items) {
+      int slot, rows, crow;
+      meta(blockIdx.x, slot, rows, crow);
+      sMeta[0][0] = slot;
+      sMeta[0][1] = rows;
+      sMeta[0][2] = crow;
+      issue_state(blockIdx.x, slot, rows);  // before the prologue has finished
     }
-    for (int s = 0; s < 2; ++s) {  // state slices of the first two items: before the prologue ends
-      const int it = blockIdx.x + s * gridDim.x;
-      int slot = 0, rows = 0, crow = -1;
-      if (it < n_items) meta(it, slot, rows, crow);
-      sMeta[s][0] = slot;
-      sMeta[s][1] = rows;
-      sMeta[s][2] = crow;
-      if (rows > 0)
-        issue_state(s, it, slot);
-      else
-        mbar_arrive(&barS[s]);
-    }
+    if (blockIdx.x + gridDim.x < n_items) meta(blockIdx.x + gridDim.x, nslot, nrows, ncrow);
   }
-  pdl_wait();  // the prologue's q, k, v and scalars are complete and visible
-  if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      const int it = blockIdx.x + s * gridDim.x;
-      if (sMeta[s][1] > 0)
-        issue_rows(s, it, sMeta[s][1]);
-      else
-        mbar_arrive(&barQ[s]);
-    }
-  }
-  __syncthreads();
+  __syncthreads();  // the barriers are initialised before anyone waits on them
+  pdl_wait();       // the prologue's q, k, v and scalars are complete and visible
+  if (tid == 0 && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1]);
 
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
@@ -490,131 +492,124 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const int it = blockIdx.x + k * gridDim.x;
     if (it >= n_items) break;
     const int s = k & 1;
-    const uint32_t ph = (k >> 1) & 1;
-    const int slot = sMeta[s][0], rows = sMeta[s][1], a = sMeta[s][2];
-    // producer: meta of the item two ahead, in flight while this one runs
-    const int it2 = it + 2 * gridDim.x;
-    int slot2 = 0, rows2 = 0, crow2 = -1;
-    if (tid == 0 && it2 < n_items) meta(it2, slot2, rows2, crow2);
-
-    const bool late = !(mbar_wait(&barS[s], ph) && mbar_wait(&barQ[s], ph));
+    // the arrive that completes each phase releases the producer's sMeta write
+    const bool late = !(mbar_wait(&barS, k & 1) && mbar_wait(&barQ[s], (k >> 1) & 1));
     if (__syncthreads_or(late)) {
       if (tid == 0) flag(p.status, GDN_STATUS_TIMEOUT);
-      mbar_wait(&barS[s], ph);  // bounded: let copies still in flight land before leaving
-      mbar_wait(&barQ[s], ph);
-      mbar_wait(&barS[s ^ 1], ph ^ (s ? 1u : 0u));
-      mbar_wait(&barQ[s ^ 1], ph ^ (s ? 1u : 0u));
+      mbar_wait(&barS, k & 1);  // bounded: let copies still in flight land before leaving
+      mbar_wait(&barQ[s], (k >> 1) & 1);
       return;
     }
+    const int slot = sMeta[s][0], rows = sMeta[s][1], a = sMeta[s][2];
 
+    f2 S[M][2 * NC4];  // column pairs of the lane's 4-column chunks
     if (rows > 0) {
-      const int b = it / (p.H_v * p.slices);
-      const int hs = it - b * p.H_v * p.slices;
-      const int h = hs / p.slices, sl = hs - h * p.slices;
-      // ---- state slice: shared memory -> registers ----
-      const float* sS = stS(s);
-      f2 S[M][2 * NC4];  // column pairs of the lane's 4-column chunks
 #pragma unroll
       for (int m = 0; m < M; ++m)
 #pragma unroll
         for (int j = 0; j < NC4; ++j) {
-          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(sS + (wrow + m * RG) * DK + 4 * (c + LPR * j));
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(stS + (wrow + m * RG) * DK + 4 * (c + LPR * j));
           S[m][2 * j] = v.x;
           S[m][2 * j + 1] = v.y;
         }
-      const float* sQK = stQK(s);
-      const float* sV = stV(s);
-      const float* sSC = stSC(s);
-      float* Sg = p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK;
-      float* og = nullptr;
-      if (kWantO) og = p.o + ((size_t)b * R * p.H_v + h) * p.d_v + (size_t)sl * DVS;
-
-      for (int t = 0; t < rows; ++t) {
-        const float4 sc = *reinterpret_cast<const float4*>(sSC + 4 * t);  // alpha, beta, k.q
-        const float alpha = sc.x, bt = sc.y;
-        const f2 alpha2 = pack2(alpha, alpha);
-        const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + DK);
-        f2 kv[2 * NC4];
-#pragma unroll
-        for (int j = 0; j < NC4; ++j) {
-          const ulonglong2 v = k4[c + LPR * j];
-          kv[2 * j] = v.x;
-          kv[2 * j + 1] = v.y;
-        }
-        float part_v[V];
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-          f2 acc = fma2(S[m][0], kv[0], pack2(0.f, 0.f));
-#pragma unroll
-          for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], kv[j], acc);
-          part_v[m] = sum2(acc);
-        }
-        if constexpr (kWantO) {
-          const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK);
-          f2 qv[2 * NC4];
-#pragma unroll
-          for (int j = 0; j < NC4; ++j) {
-            const ulonglong2 v = q4[c + LPR * j];
-            qv[2 * j] = v.x;
-            qv[2 * j + 1] = v.y;
-          }
-#pragma unroll
-          for (int m = 0; m < M; ++m) {
-            f2 acc = fma2(S[m][0], qv[0], pack2(0.f, 0.f));
-#pragma unroll
-            for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], qv[j], acc);
-            part_v[(M + m) % V] = sum2(acc);
-          }
-        }
-        int idx;
-        const float red = reduce_scatter<LPR, V>(part_v, lane, idx);
-        const int mrow = idx % M;
-        const int rloc = wrow + mrow * RG;
-        // u is meaningful on the lanes holding an S k sum (idx < M)
-        const float u = __fmul_rn(bt, __fsub_rn(sV[t * DVS + rloc], __fmul_rn(alpha, red)));
-        if constexpr (kWantO) {
-          const float up = __shfl_xor_sync(kFull, u, LPR / 2);  // u of the same row
-          if (idx >= M && (c & kDupMask) == 0)
-            og[(size_t)t * o_tstride + rloc] = __fmaf_rn(up, sc.z, __fmul_rn(alpha, red));
-        }
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-          const float um = __shfl_sync(kFull, u, gbase | value_lane<LPR, V>(m));
-          const f2 u2 = pack2(um, um);
-#pragma unroll
-          for (int j = 0; j < 2 * NC4; ++j) S[m][j] = fma2(u2, kv[j], mul2(alpha2, S[m][j]));
-        }
-
-        if (kCommits && t == a) {
-#pragma unroll
-          for (int m = 0; m < M; ++m)
-#pragma unroll
-            for (int j = 0; j < NC4; ++j)
-              *reinterpret_cast<ulonglong2*>(Sg + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
-                  make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
-        }
-        if (kSnap) {
-          float* Ss = p.snapS + (((size_t)b * R + t) * p.H_v * p.slices + hs) * DVS * DK;
-#pragma unroll
-          for (int m = 0; m < M; ++m)
-#pragma unroll
-            for (int j = 0; j < NC4; ++j)
-              *reinterpret_cast<ulonglong2*>(Ss + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
-                  make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
-        }
+    }
+    __syncthreads();  // the state buffer is free: request the next item
+    if (tid == 0) {
+      const int it1 = it + gridDim.x;
+      if (it1 < n_items) {
+        fence_proxy_async();  // the reads above happen before the bulk copies overwrite the buffers
+        sMeta[s ^ 1][0] = nslot;
+        sMeta[s ^ 1][1] = nrows;
+        sMeta[s ^ 1][2] = ncrow;
+        issue_state(it1, nslot, nrows);
+        issue_rows(s ^ 1, it1, nrows);
+        if (it1 + gridDim.x < n_items) meta(it1 + gridDim.x, nslot, nrows, ncrow);  // in flight meanwhile
       }
     }
-    __syncthreads();  // stage s is consumed: refill it with the item two ahead
-    if (tid == 0 && it2 < n_items) {
-      sMeta[s][0] = slot2;
-      sMeta[s][1] = rows2;
-      sMeta[s][2] = crow2;
-      if (rows2 > 0) {
-        issue_state(s, it2, slot2);
-        issue_rows(s, it2, rows2);
-      } else {
-        mbar_arrive(&barS[s]);
-        mbar_arrive(&barQ[s]);
+    if (rows == 0) continue;
+
+    const int b = it / (p.H_v * p.slices);
+    const int hs = it - b * p.H_v * p.slices;
+    const int h = hs / p.slices, sl = hs - h * p.slices;
+    const float* sQK = stQK(s);
+    const float* sV = stV(s);
+    const float* sSC = stSC(s);
+    float* Sg = p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK;
+    float* og = nullptr;
+    if (kWantO) og = p.o + ((size_t)b * R * p.H_v + h) * p.d_v + (size_t)sl * DVS;
+
+    for (int t = 0; t < rows; ++t) {
+      const float4 sc = *reinterpret_cast<const float4*>(sSC + 4 * t);  // alpha, beta, k.q
+      const float alpha = sc.x, bt = sc.y;
+      const f2 alpha2 = pack2(alpha, alpha);
+      const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + DK);
+      f2 kv[2 * NC4];
+#pragma unroll
+      for (int j = 0; j < NC4; ++j) {
+        const ulonglong2 v = k4[c + LPR * j];
+        kv[2 * j] = v.x;
+        kv[2 * j + 1] = v.y;
+      }
+      float part_v[V];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        f2 acc = fma2(S[m][0], kv[0], pack2(0.f, 0.f));
+#pragma unroll
+        for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], kv[j], acc);
+        part_v[m] = sum2(acc);
+      }
+      if constexpr (kWantO) {
+        const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK);
+        f2 qv[2 * NC4];
+#pragma unroll
+        for (int j = 0; j < NC4; ++j) {
+          const ulonglong2 v = q4[c + LPR * j];
+          qv[2 * j] = v.x;
+          qv[2 * j + 1] = v.y;
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          f2 acc = fma2(S[m][0], qv[0], pack2(0.f, 0.f));
+#pragma unroll
+          for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], qv[j], acc);
+          part_v[(M + m) % V] = sum2(acc);
+        }
+      }
+      int idx;
+      const float red = reduce_scatter<LPR, V>(part_v, lane, idx);
+      const int mrow = idx % M;
+      const int rloc = wrow + mrow * RG;
+      // u is meaningful on the lanes holding an S k sum (idx < M)
+      const float u = __fmul_rn(bt, __fsub_rn(sV[t * DVS + rloc], __fmul_rn(alpha, red)));
+      if constexpr (kWantO) {
+        const float up = __shfl_xor_sync(kFull, u, LPR / 2);  // u of the same row
+        if (idx >= M && (c & kDupMask) == 0)
+          og[(size_t)t * o_tstride + rloc] = __fmaf_rn(up, sc.z, __fmul_rn(alpha, red));
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float um = __shfl_sync(kFull, u, gbase | value_lane<LPR, V>(m));
+        const f2 u2 = pack2(um, um);
+#pragma unroll
+        for (int j = 0; j < 2 * NC4; ++j) S[m][j] = fma2(u2, kv[j], mul2(alpha2, S[m][j]));
+      }
+
+      if (kCommits && t == a) {
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+          for (int j = 0; j < NC4; ++j)
+            *reinterpret_cast<ulonglong2*>(Sg + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
+                make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+      }
+      if (kSnap) {
+        float* Ss = p.snapS + (((size_t)b * R + t) * p.H_v * p.slices + hs) * DVS * DK;
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+          for (int j = 0; j < NC4; ++j)
+            *reinterpret_cast<ulonglong2*>(Ss + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
+                make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
       }
     }
   }
@@ -661,12 +656,12 @@ int launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, c
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
-// Persistent grid of the rows kernel: as many CTAs as fit at once, trimmed so
-// every CTA runs the same number of items.
+// Persistent grid of the rows kernel: as many CTAs as fit at once (at most one
+// per item).
 template <int DK, int MODE>
 int launch_rows(const Params& p, cudaStream_t st) {
   using Gm = Geo<DK>;
-  const size_t smem = 2 * sizeof(float) * (size_t)Stage<DK>::floats(p.R);
+  const size_t smem = Stage<DK>::bytes(p.R);
   struct Cache {
     int dev = -1;
     size_t smem = 0;
@@ -689,8 +684,7 @@ int launch_rows(const Params& p, cudaStream_t st) {
     cache.ctas = per_sm * sms;
   }
   const long long items = (long long)p.B * p.H_v * p.slices;
-  const long long per_cta = (items + cache.ctas - 1) / cache.ctas;
-  const int grid = (int)((items + per_cta - 1) / per_cta);
+  const int grid = (int)(items < cache.ctas ? items : cache.ctas);
   return launch(rows_kernel<DK, MODE>, dim3(grid), dim3(Gm::NT), smem, st, p);
 }
 
