@@ -147,11 +147,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CUDA arm
-def build_stack(layers: int, device: str):
+def build_stack(layers: int, device: str, batch: int | None = None):
+    from dataclasses import replace
+
     from speculative_decode_gateddeltanet_gb300 import gdn
 
     host, devs = [], []
     for spec, seed in workload_layers(STACK, layers=layers):
+        if batch is not None and batch != spec.B:
+            spec = replace(spec, B=batch, name=f"qwen35-{layers}L-B{batch}-k{spec.k}")
         layer = make_layer(spec, seed)
         host.append(layer)
         devs.append(gdn.DeviceLayer(layer, device, snapshot=False))
@@ -166,7 +170,7 @@ def run_cuda(args, rank, ws, local):
 
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    host, devs = build_stack(args.layers, device)
+    host, devs = build_stack(args.layers, device, args.batch)
     spec = host[0]["spec"]
     if args.mode == "snapshot":
         for d in devs:
@@ -346,6 +350,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--mode", choices=["fused", "replay", "snapshot"], default="fused")
     ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--batch", type=int, default=None, help="requests per layer (default: the workload's 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

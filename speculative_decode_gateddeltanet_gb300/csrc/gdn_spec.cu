@@ -258,14 +258,14 @@ __device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, i
 //   wqk [B][H_qk][R][2 d_k]   scale*q^ | k^       (one contiguous run per (b, q/k head))
 //   wv  [B][H_v d_v/DVS][R][DVS]  v               (one run per (b, head, row slice))
 //   wsc [B][H_v][R][4]        exp(g), beta, k^.(scale q^), 0   (one run per (b, head))
-template <typename T, int MODE>
+template <typename T, int MODE, int RMAX>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
   constexpr bool kSnap = MODE == kVerifySnap;
   pdl_wait();     // whatever ran before on the stream is complete and visible
   pdl_trigger();  // the rows kernel may start loading its state
-  __shared__ float sy[kMaxR][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
-  __shared__ float sf[kMaxR][3];             // q/k blocks: fq, fk, k^.(scale q^) per row
+  __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
+  __shared__ float sf[RMAX][3];             // q/k blocks: fq, fk, k^.(scale q^) per row
 
   const int b = blockIdx.y;
   int slot, a, report;
@@ -301,9 +301,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     const T* wg = static_cast<const T*>(p.conv_w) + ch * kW;
     T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
     // every load first, so they are all in flight together
-    T xr[kMaxR];
+    T xr[RMAX];
 #pragma unroll
-    for (int t = 0; t < kMaxR; ++t)
+    for (int t = 0; t < RMAX; ++t)
       if (t < t_end) xr[t] = xg[(size_t)t * p.C];
     const T q0 = wg[0], q1 = wg[1], q2 = wg[2], q3 = wg[3];
     T r0 = cs[0], r1 = cs[1], r2 = cs[2];  // window, oldest first, kept as stored
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     if (!qk_block)
       vdst = p.wv + (((size_t)b * p.H_v * p.slices + vi / p.dvs) * p.R) * p.dvs + (vi % p.dvs);
 #pragma unroll
-    for (int t = 0; t < kMaxR; ++t) {
+    for (int t = 0; t < RMAX; ++t) {
       if (t < t_end) {
         const T r3 = xr[t];
         float z = __fmul_rn(w0, tof(r0));
@@ -702,12 +702,18 @@ int dispatch_rows(const Params& p, cudaStream_t st) {
   }
 }
 
+template <typename T, int MODE>
+int launch_prep(const Params& p, cudaStream_t st) {
+  const dim3 grid(p.H_qk + (p.H_v * p.d_v + kPrepThreads - 1) / kPrepThreads, p.B), block(kPrepThreads);
+  if (p.R <= 4) return launch(prep_kernel<T, MODE, 4>, grid, block, 0, st, p);
+  if (p.R <= 8) return launch(prep_kernel<T, MODE, 8>, grid, block, 0, st, p);
+  return launch(prep_kernel<T, MODE, kMaxR>, grid, block, 0, st, p);
+}
+
 template <int MODE>
 int run_mode(const Params& p, int in_dtype, cudaStream_t st) {
-  const dim3 pgrid(p.H_qk + (p.H_v * p.d_v + kPrepThreads - 1) / kPrepThreads, p.B);
-  const int rc = in_dtype == GDN_DTYPE_BF16
-                     ? launch(prep_kernel<__nv_bfloat16, MODE>, pgrid, dim3(kPrepThreads), 0, st, p)
-                     : launch(prep_kernel<float, MODE>, pgrid, dim3(kPrepThreads), 0, st, p);
+  const int rc = in_dtype == GDN_DTYPE_BF16 ? launch_prep<__nv_bfloat16, MODE>(p, st)
+                                            : launch_prep<float, MODE>(p, st);
   if (rc != GDN_OK) return rc;
   return dispatch_rows<MODE>(p, st);
 }
