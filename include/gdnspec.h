@@ -39,8 +39,8 @@
  *   scratch_cs  [B][R][C][W-1]        in_dtype   snapshot mode: conv window after row t
  *   work        gdn_work_bytes(args) bytes       the call's own scratch: per row the
  *                                                normalised q and k of every q/k head, v,
- *                                                decay, write strength and k.q; contents on
- *                                                entry do not matter
+ *                                                decay and write strength, and the rows'
+ *                                                Gram tables; contents on entry do not matter
  *   status      [1]                   int32      device word; error bits are OR-ed in, never cleared
  *
  * Supported: W = 4; d_k in {16, 32, 64, 128}; d_v a multiple of 16 (d_k = 16)
@@ -151,7 +151,8 @@ GDN_API int gdn_commit(const gdn_args* args, int mode, void* stream);
 GDN_API int gdn_verify_commit(const gdn_args* args, void* stream);
 
 /* Bytes of `work` a verify, replay commit or fused call with these shapes
- * needs: 4 * B * R * (2 * H_qk * d_k + H_v * d_v + 4 * H_v).  Reads only the
+ * needs: 4 * (B * R * (2 * H_qk * d_k + H_v * d_v + 4 * H_v) + B * H_qk * G2), with
+ * G2 = 2 * R * R rounded up to a multiple of 4.  Reads only the
  * size fields of args; 0 if they are invalid or unsupported. */
 GDN_API size_t gdn_work_bytes(const gdn_args* args);
 

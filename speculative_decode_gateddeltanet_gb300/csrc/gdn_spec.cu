@@ -5,8 +5,9 @@
 //
 // prep_kernel (one thread per channel): the width-4 causal conv + SiLU of
 //   every row over [committed window | verify rows], then the per-head L2
-//   norm of q and k.  Writes scale*q^, k^, v and k^.(scale q^) per row into
-//   the caller's work buffer.  Each conv channel has exactly one reader in
+//   norm of q and k.  Writes scale*q^, k^, v, the decay and write strength
+//   per row, and the rows' Gram tables k^.k^ and k^.(scale q^) into the
+//   caller's work buffer.  Each conv channel has exactly one reader in
 //   the call, so that thread also writes the channel's committed window
 //   (commit modes) or its per-row windows (snapshot mode).  The conv reads
 //   only the committed window and the verify rows, staging [history | verify
@@ -16,22 +17,19 @@
 // rows_kernel (one CTA per (request, value head, slice of DVS state rows)):
 //   loads its slice of the fp32 state S (DVS x d_k, d_k contiguous) with
 //   128-bit loads into registers before waiting on the prologue, stages the
-//   rows' q, k, v from the work buffer with bulk async copies, and runs the
-//   rows with S resident in registers.  Per row t, with alpha = exp(g_t) and
-//   packed f32x2 arithmetic:
-//     r = S k, p = S q~           (q~ = scale * q)       on the old S
-//     u = beta (v - alpha r)
-//     o = alpha p + u (k . q~)    = scale * S_t q
-//     S <- alpha S + u k^T
-//   which is the gated delta rule S_t = alpha S + beta (v - alpha S k) k^T,
-//   o_t = scale S_t q.  Lanes own 4-float column chunks of two rows; a row's
-//   dot products are reduced over its 8 (d_k >= 32) or 4 (d_k = 16) lanes
-//   with a reduce-scatter butterfly, so each lane ends up with one finished
-//   sum.
+//   rows' q, k, v and tables from the work buffer with bulk async copies, and
+//   runs the gated delta rule S_t = alpha S + beta (v - alpha S k) k^T,
+//   o_t = scale S_t q with S resident in registers, in the chunked form
+//   described at the kernel (all dot products of a chunk of rows on the
+//   chunk's starting state, a scalar recurrence per state row, one state
+//   update).  Lanes own 4-float column chunks of 2 or 4 rows; a row's dot
+//   products are reduced over its 8 (d_k >= 32) or 4 (d_k = 16) lanes with a
+//   butterfly that leaves each lane holding one row's sums.  Arithmetic is
+//   fp32 with packed f32x2 FMA/MUL.
 //
-// The arithmetic of a row does not depend on the mode, on how many rows the
-// call has or on which rows follow, so a fused call, a verify followed by a
-// replay commit, and a chain of one-row calls give the same bits.
+// The arithmetic of a row does not depend on the mode, so a fused call, a
+// verify followed by a replay commit and a snapshot verify followed by a
+// snapshot commit give the same bits.
 //
 // Modes: verify (o only; the state is only read [FreeToken #828
 // "Speculative decoding: MTP and DFlash", Design]), verify with per-row
@@ -78,7 +76,8 @@ struct Params {
   int dvs;     // state rows per rows-kernel item
   float* wqk;  // work: [B][H_qk][R][2 d_k]         scale*q^ | k^
   float* wv;   // work: [B][H_v d_v / dvs][R][dvs]  v
-  float* wsc;  // work: [B][H_v][R][4]              exp(g), beta, k^.(scale q^), 0
+  float* wsc;  // work: [B][H_v][R][4]              exp(g), beta, 0, 0
+  float* wgh;  // work: [B][H_qk][gram_floats(R)]   [R][R][2]: k^_s . k^_t, k^_s . (scale q^_t)
   int* status;
 };
 
@@ -97,6 +96,9 @@ struct Geo {
 };
 
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+// Floats of one (request, q/k head) Gram table [R][R][2], padded to 16 bytes so
+// every table starts and ends on a bulk-copy boundary.
+__host__ __device__ constexpr int gram_floats(int R) { return (2 * R * R + 3) & ~3; }
 
 // ---- packed fp32 pairs (f32x2) ----
 typedef unsigned long long f2;
@@ -129,46 +131,6 @@ template <>
 __device__ __forceinline__ float tof<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 __device__ __forceinline__ float silu(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, expf(-z))); }
-
-// Sum each of a lane's V values over the LPR lanes of its row group.  The
-// first log2(V) butterfly levels halve the values a lane carries (it keeps
-// one half and trades the other), the remaining levels are all-reduce steps.
-// On return the lane holds the finished sum of value `idx`.  The summation
-// tree of a value (partners at LPR/2, LPR/4, .., 1) is the same for every V.
-template <int LPR, int V>
-__device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane, int& idx) {
-  constexpr int kHalvings = ilog2(V);
-  static_assert((1 << kHalvings) == V && V <= LPR, "V must be a power of two <= LPR");
-  idx = 0;
-#pragma unroll
-  for (int l = 0; l < kHalvings; ++l) {
-    const int off = LPR >> (l + 1);
-    const int half = V >> (l + 1);
-    const bool up = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = up ? v[i] : v[i + half];
-      const float keep = up ? v[i + half] : v[i];
-      v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
-    }
-    if (up) idx += half;
-  }
-#pragma unroll
-  for (int off = LPR >> (kHalvings + 1); off >= 1; off >>= 1)
-    v[0] = __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], off));
-  return v[0];
-}
-
-// Offset, within a row group, of a lane that holds value `idx` after
-// reduce_scatter<LPR, V>.
-template <int LPR, int V>
-__device__ __forceinline__ int value_lane(int idx) {
-  int off = 0;
-#pragma unroll
-  for (int l = 0; (V >> (l + 1)) >= 1; ++l)
-    if ((idx / (V >> (l + 1))) & 1) off |= LPR >> (l + 1);
-  return off;
-}
 
 __device__ __forceinline__ void flag(int* status, int bit) {
   if (status) atomicOr(status, bit);
@@ -265,7 +227,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   pdl_wait();     // whatever ran before on the stream is complete and visible
   pdl_trigger();  // the rows kernel may start loading its state
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
-  __shared__ float sf[RMAX][3];             // q/k blocks: fq, fk, k^.(scale q^) per row
+  __shared__ float sf[RMAX][2];             // q/k blocks: fq, fk per row
 
   const int b = blockIdx.y;
   int slot, a, report;
@@ -351,33 +313,46 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   __syncthreads();
   // per-row L2 norms of q and k, one warp per row
   for (int t = warp; t < t_end; t += kPrepThreads / 32) {
-    float sq = 0.f, sk = 0.f, qk = 0.f;
+    float sq = 0.f, sk = 0.f;
     for (int e = lane; e < DK; e += 32) {
       const float qv = sy[t][e], kv = sy[t][DK + e];
       sq = __fmaf_rn(qv, qv, sq);
       sk = __fmaf_rn(kv, kv, sk);
-      qk = __fmaf_rn(qv, kv, qk);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       sq = __fadd_rn(sq, __shfl_xor_sync(kFull, sq, off));
       sk = __fadd_rn(sk, __shfl_xor_sync(kFull, sk, off));
-      qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, off));
     }
     if (lane == 0) {
       const float fq = __fmul_rn(p.scale, rsqrtf(__fadd_rn(sq, p.eps)));
       const float fk = rsqrtf(__fadd_rn(sk, p.eps));
       sf[t][0] = fq;
       sf[t][1] = fk;
-      sf[t][2] = __fmul_rn(__fmul_rn(qk, fq), fk);
     }
   }
   __syncthreads();
-  if (active) {
+  if (active) {  // normalise in place and publish scale*q^ | k^
     float* dst = p.wqk + ((size_t)b * p.H_qk + hq) * p.R * 2 * DK + tid;
-    for (int t = 0; t < t_end; ++t) dst[(size_t)t * 2 * DK] = __fmul_rn(sy[t][tid], sf[t][tid < DK ? 0 : 1]);
+    for (int t = 0; t < t_end; ++t) {
+      const float y = __fmul_rn(sy[t][tid], sf[t][tid < DK ? 0 : 1]);
+      sy[t][tid] = y;
+      dst[(size_t)t * 2 * DK] = y;
+    }
   }
-  // per-row scalars of the value heads that read this q/k head
+  __syncthreads();
+  // Gram tables of the rows: k^_s . k^_t and k^_s . (scale q^_t), one warp per entry
+  float* gh = p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(p.R);
+  for (int e = warp; e < 2 * p.R * p.R; e += kPrepThreads / 32) {
+    const int which = e & 1, st = e >> 1, s0 = st / p.R, t0 = st % p.R;
+    float acc = 0.f;
+    if (s0 < t_end && t0 < t_end)
+      for (int j = lane; j < DK; j += 32) acc = __fmaf_rn(sy[s0][DK + j], sy[t0][which ? j : DK + j], acc);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
+    if (lane == 0) gh[e] = acc;
+  }
+  // per-row decay and write strength of the value heads that read this q/k head
   for (int i = tid; i < p.G * t_end; i += kPrepThreads) {
     const int h = hq * p.G + i / t_end, t = i % t_end;
     if (i >= kPrepThreads) {  // more (head, row) pairs than threads: load now
@@ -386,7 +361,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
       beta_i = __ldg(p.beta + gi);
     }
     *reinterpret_cast<float4*>(p.wsc + (((size_t)b * p.H_v + h) * p.R + t) * 4) =
-        make_float4(expf(g_i), beta_i, sf[t][2], 0.f);
+        make_float4(expf(g_i), beta_i, 0.f, 0.f);
   }
 }
 
@@ -395,25 +370,83 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
 // value head h, row slice sl), numbered ((b H_v) + h) slices + sl.  The state
 // slice has one shared-memory buffer: as soon as an item's slice is in
 // registers, the next item's slice (one bulk copy) is requested, so it is in
-// flight while the item computes.  The item's q/k rows, v rows and per-row
-// scalars are small and double-buffered.
+// flight while the item computes.  The item's q/k rows, v rows, per-row
+// scalars and Gram tables are small and double-buffered.
+//
+// The rows of an item run in chunks of up to CH rows.  With C_t the product of
+// the decays of the chunk's rows up to t and z_s^(t) = (C_t / C_s) u_s, the
+// recurrence unrolls over the chunk to
+//   r_t = C_t (S0 k_t) + sum_{s<t} z_s^(t-1) alpha_t (k_s . k_t)      u_t = beta_t (v_t - r_t)
+//   o_t = C_t (S0 q~_t) + sum_{s<=t} z_s^(t) (k_s . q~_t)
+//   S_t = C_t S0 + sum_{s<=t} z_s^(t) k_s^T
+// so every dot product of the chunk is taken on the chunk's starting state S0
+// in one pass, each state row then runs a short scalar recurrence, and the
+// state is written once (at the commit row, or advanced to the chunk's end).
 template <int DK>
 struct Stage {
   static constexpr int DVS = Geo<DK>::DVS;
-  __host__ __device__ static int rows_floats(int R) { return R * 2 * DK + R * DVS + R * 4; }
+  __host__ __device__ static int rows_floats(int R) { return R * 2 * DK + R * DVS + R * 4 + gram_floats(R); }
   __host__ __device__ static size_t bytes(int R) { return sizeof(float) * ((size_t)DVS * DK + 2 * (size_t)rows_floats(R)); }
 };
+
+// Sums, over the LPR lanes of a row group, each lane's partial dot products of
+// its M rows with NV vectors (v[m][x]), and leaves the lane holding the NV
+// finished sums of one row: row_of_lane<LPR, M>(lane).  Partners are taken at
+// offsets LPR/2, LPR/4, .., 1 in that order, the same for every value.
+template <int LPR, int M, int NV>
+__device__ __forceinline__ void reduce_rows(float (&v)[M][NV], float (&out)[NV], int lane) {
+  constexpr int LM = ilog2(M);
+  static_assert((1 << LM) == M && M <= LPR, "M must be a power of two <= LPR");
+#pragma unroll
+  for (int l = 0; l < LM; ++l) {
+    const int off = LPR >> (l + 1);
+    const int half = M >> (l + 1);
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i)
+#pragma unroll
+      for (int x = 0; x < NV; ++x) {
+        const float send = up ? v[i][x] : v[i + half][x];
+        const float keep = up ? v[i + half][x] : v[i][x];
+        v[i][x] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
+      }
+  }
+#pragma unroll
+  for (int off = LPR >> (LM + 1); off >= 1; off >>= 1)
+#pragma unroll
+    for (int x = 0; x < NV; ++x) v[0][x] = __fadd_rn(v[0][x], __shfl_xor_sync(kFull, v[0][x], off));
+#pragma unroll
+  for (int x = 0; x < NV; ++x) out[x] = v[0][x];
+}
+template <int LPR, int M>
+__device__ __forceinline__ int row_of_lane(int lane) {
+  int m = 0;
+#pragma unroll
+  for (int l = 0; l < ilog2(M); ++l)
+    if (lane & (LPR >> (l + 1))) m += M >> (l + 1);
+  return m;
+}
+// offset within the row group of a lane that holds row m's sums
+template <int LPR, int M>
+__device__ __forceinline__ int lane_of_row(int m) {
+  int off = 0;
+#pragma unroll
+  for (int l = 0; l < ilog2(M); ++l)
+    if ((m / (M >> (l + 1))) & 1) off |= LPR >> (l + 1);
+  return off;
+}
 
 template <int DK, int MODE>
 __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(const Params p) {
   using Gm = Geo<DK>;
   constexpr int LPR = Gm::LPR, NC4 = Gm::NC4, RG = Gm::RG, M = Gm::M;
   constexpr int DVS = Gm::DVS, ROWS_W = Gm::ROWS_W;
+  constexpr int NP = 2 * NC4;  // column pairs per lane per row
+  constexpr int CH = 4;        // rows per chunk
+  constexpr int kDup = (LPR >> ilog2(M)) - 1;  // low lane bits that repeat a row's sums
   constexpr bool kWantO = MODE != kCommitReplay;
   constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
   constexpr bool kSnap = MODE == kVerifySnap;
-  constexpr int V = kWantO ? 2 * M : M;
-  constexpr int kDupMask = (LPR >> ilog2(V)) - 1;  // lanes that repeat a finished sum
   constexpr uint32_t kSBytes = DVS * DK * sizeof(float);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -422,9 +455,10 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   const int rfl = Stage<DK>::rows_floats(R);
   extern __shared__ __align__(16) float smem[];
   float* const stS = smem;  // [DVS][DK] state slice of the next item
-  auto stQK = [&](int s) { return smem + DVS * DK + (size_t)s * rfl; };  // [R][2 DK]
-  auto stV = [&](int s) { return stQK(s) + R * 2 * DK; };               // [R][DVS]
-  auto stSC = [&](int s) { return stV(s) + R * DVS; };                  // [R][4]
+  auto stQK = [&](int s) { return smem + DVS * DK + (size_t)s * rfl; };  // [R][2 DK]  scale*q^ | k^
+  auto stV = [&](int s) { return stQK(s) + R * 2 * DK; };               // [R][DVS]   v
+  auto stSC = [&](int s) { return stV(s) + R * DVS; };                  // [R][4]     exp(g), beta
+  auto stGH = [&](int s) { return stSC(s) + R * 4; };                   // [R][R][2]  k.k, k.q~ (padded)
   __shared__ __align__(8) uint64_t barS, barQ[2];
   __shared__ int sMeta[2][3];  // per item parity: slot, rows to run, commit row (-1 none)
 
@@ -457,10 +491,12 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const int hs = it - b * p.H_v * p.slices;
     const int h = hs / p.slices;
     const int hq = h / p.G;
-    mbar_expect_tx(&barQ[s], (uint32_t)(rows * (2 * DK + DVS + 4) * sizeof(float)));
+    mbar_expect_tx(&barQ[s], (uint32_t)((rows * (2 * DK + DVS + 4) + gram_floats(R)) * sizeof(float)));
     bulk_load(stQK(s), p.wqk + ((size_t)b * p.H_qk + hq) * R * 2 * DK, rows * 2 * DK * sizeof(float), &barQ[s]);
     bulk_load(stV(s), p.wv + ((size_t)b * p.H_v * p.slices + hs) * R * DVS, rows * DVS * sizeof(float), &barQ[s]);
     bulk_load(stSC(s), p.wsc + ((size_t)b * p.H_v + h) * R * 4, rows * 4 * sizeof(float), &barQ[s]);
+    bulk_load(stGH(s), p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(R), gram_floats(R) * sizeof(float),
+              &barQ[s]);
   };
 
   int nslot = 0, nrows = 0, ncrow = -1;  // producer: meta of the item after the current one
@@ -479,13 +515,15 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     if (blockIdx.x + gridDim.x < n_items) meta(blockIdx.x + gridDim.x, nslot, nrows, ncrow);
   }
   __syncthreads();  // the barriers are initialised before anyone waits on them
-  pdl_wait();       // the prologue's q, k, v and scalars are complete and visible
+  pdl_wait();       // the prologue's q, k, v and tables are complete and visible
   if (tid == 0 && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1]);
 
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
   const int wrow = warp * ROWS_W + rg;  // slice-local row of m = 0; row m adds m * RG
   const int gbase = lane & ~(LPR - 1);
+  const int rl = wrow + row_of_lane<LPR, M>(lane) * RG;  // the row whose sums this lane holds
+  const bool writer = (lane & kDup) == 0;
   const size_t o_tstride = (size_t)p.H_v * p.d_v;
 
   for (int k = 0;; ++k) {
@@ -502,7 +540,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     }
     const int slot = sMeta[s][0], rows = sMeta[s][1], a = sMeta[s][2];
 
-    f2 S[M][2 * NC4];  // column pairs of the lane's 4-column chunks
+    f2 S[M][NP];  // column pairs of the lane's 4-column chunks
     if (rows > 0) {
 #pragma unroll
       for (int m = 0; m < M; ++m)
@@ -534,83 +572,173 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const float* sQK = stQK(s);
     const float* sV = stV(s);
     const float* sSC = stSC(s);
+    const float* sGH = stGH(s);
     float* Sg = p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK;
     float* og = nullptr;
-    if (kWantO) og = p.o + ((size_t)b * R * p.H_v + h) * p.d_v + (size_t)sl * DVS;
+    if (kWantO) og = p.o + ((size_t)b * R * p.H_v + h) * p.d_v + (size_t)sl * DVS + rl;
 
-    for (int t = 0; t < rows; ++t) {
-      const float4 sc = *reinterpret_cast<const float4*>(sSC + 4 * t);  // alpha, beta, k.q
-      const float alpha = sc.x, bt = sc.y;
-      const f2 alpha2 = pack2(alpha, alpha);
-      const ulonglong2* k4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + DK);
-      f2 kv[2 * NC4];
+    // lane's column pairs of row vector t (q at offset 0, k at offset DK)
+    auto load_vec = [&](int t, int off, f2 (&vv)[NP]) {
+      const ulonglong2* vp = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + off);
 #pragma unroll
       for (int j = 0; j < NC4; ++j) {
-        const ulonglong2 v = k4[c + LPR * j];
-        kv[2 * j] = v.x;
-        kv[2 * j + 1] = v.y;
+        const ulonglong2 v = vp[c + LPR * j];
+        vv[2 * j] = v.x;
+        vv[2 * j + 1] = v.y;
       }
-      float part_v[V];
+    };
+    // dst[m] = cc * S[m] + sum_{s<nt} w_s(row m) k_{c0+s}, in that order; in place when dst is S
+    auto combine = [&](int c0, int nt, float cc, const float (&w)[CH], bool in_place, float* out) {
+      // coefficient x of row m lives in the lane holding row m's sums
+      auto wm = [&](int m, int x) { return __shfl_sync(kFull, w[x], gbase | lane_of_row<LPR, M>(m)); };
+      const f2 cc2 = pack2(cc, cc);
+      if (in_place) {
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        f2 acc = fma2(S[m][0], kv[0], pack2(0.f, 0.f));
+        for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], kv[j], acc);
-        part_v[m] = sum2(acc);
-      }
-      if constexpr (kWantO) {
-        const ulonglong2* q4 = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK);
-        f2 qv[2 * NC4];
+          for (int j = 0; j < NP; ++j) S[m][j] = mul2(cc2, S[m][j]);
 #pragma unroll
-        for (int j = 0; j < NC4; ++j) {
-          const ulonglong2 v = q4[c + LPR * j];
-          qv[2 * j] = v.x;
-          qv[2 * j + 1] = v.y;
+        for (int x = 0; x < CH; ++x) {
+          if (x < nt) {
+            f2 kv[NP];
+            load_vec(c0 + x, DK, kv);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              const float wx = wm(m, x);
+              const f2 w2 = pack2(wx, wx);
+#pragma unroll
+              for (int j = 0; j < NP; ++j) S[m][j] = fma2(w2, kv[j], S[m][j]);
+            }
+          }
         }
+      } else {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          f2 acc = fma2(S[m][0], qv[0], pack2(0.f, 0.f));
+          f2 acc[NP];
 #pragma unroll
-          for (int j = 1; j < 2 * NC4; ++j) acc = fma2(S[m][j], qv[j], acc);
-          part_v[(M + m) % V] = sum2(acc);
+          for (int j = 0; j < NP; ++j) acc[j] = mul2(cc2, S[m][j]);
+#pragma unroll
+          for (int x = 0; x < CH; ++x) {
+            if (x < nt) {
+              f2 kv[NP];
+              load_vec(c0 + x, DK, kv);
+              const float wx = wm(m, x);
+              const f2 w2 = pack2(wx, wx);
+#pragma unroll
+              for (int j = 0; j < NP; ++j) acc[j] = fma2(w2, kv[j], acc[j]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < NC4; ++j)
+            *reinterpret_cast<ulonglong2*>(out + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
+                make_ulonglong2(acc[2 * j], acc[2 * j + 1]);
         }
       }
-      int idx;
-      const float red = reduce_scatter<LPR, V>(part_v, lane, idx);
-      const int mrow = idx % M;
-      const int rloc = wrow + mrow * RG;
-      // u is meaningful on the lanes holding an S k sum (idx < M)
-      const float u = __fmul_rn(bt, __fsub_rn(sV[t * DVS + rloc], __fmul_rn(alpha, red)));
-      if constexpr (kWantO) {
-        const float up = __shfl_xor_sync(kFull, u, LPR / 2);  // u of the same row
-        if (idx >= M && (c & kDupMask) == 0)
-          og[(size_t)t * o_tstride + rloc] = __fmaf_rn(up, sc.z, __fmul_rn(alpha, red));
-      }
+    };
+    auto store_state = [&](float* out) {
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const float um = __shfl_sync(kFull, u, gbase | value_lane<LPR, V>(m));
-        const f2 u2 = pack2(um, um);
+      for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int j = 0; j < 2 * NC4; ++j) S[m][j] = fma2(u2, kv[j], mul2(alpha2, S[m][j]));
-      }
+        for (int j = 0; j < NC4; ++j)
+          *reinterpret_cast<ulonglong2*>(out + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
+              make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+    };
 
-      if (kCommits && t == a) {
+    for (int c0 = 0; c0 < rows; c0 += CH) {
+      const int nc = rows - c0 < CH ? rows - c0 : CH;
+      const bool last = c0 + CH >= rows;
+      // ---- every dot product of the chunk on its starting state ----
+      float pk[CH], pq[CH];
+      {
+        float part[M][CH];
 #pragma unroll
-        for (int m = 0; m < M; ++m)
+        for (int x = 0; x < CH; ++x) {
+          if (x < nc) {
+            f2 kv[NP];
+            load_vec(c0 + x, DK, kv);
 #pragma unroll
-          for (int j = 0; j < NC4; ++j)
-            *reinterpret_cast<ulonglong2*>(Sg + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
-                make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+            for (int m = 0; m < M; ++m) {
+              f2 acc = fma2(S[m][0], kv[0], pack2(0.f, 0.f));
+#pragma unroll
+              for (int j = 1; j < NP; ++j) acc = fma2(S[m][j], kv[j], acc);
+              part[m][x] = sum2(acc);
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < M; ++m) part[m][x] = 0.f;
+          }
+        }
+        reduce_rows<LPR, M, CH>(part, pk, lane);
       }
-      if (kSnap) {
-        float* Ss = p.snapS + (((size_t)b * R + t) * p.H_v * p.slices + hs) * DVS * DK;
+      if constexpr (kWantO) {
+        float part[M][CH];
 #pragma unroll
-        for (int m = 0; m < M; ++m)
+        for (int x = 0; x < CH; ++x) {
+          if (x < nc) {
+            f2 qv[NP];
+            load_vec(c0 + x, 0, qv);
 #pragma unroll
-          for (int j = 0; j < NC4; ++j)
-            *reinterpret_cast<ulonglong2*>(Ss + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
-                make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
+            for (int m = 0; m < M; ++m) {
+              f2 acc = fma2(S[m][0], qv[0], pack2(0.f, 0.f));
+#pragma unroll
+              for (int j = 1; j < NP; ++j) acc = fma2(S[m][j], qv[j], acc);
+              part[m][x] = sum2(acc);
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < M; ++m) part[m][x] = 0.f;
+          }
+        }
+        reduce_rows<LPR, M, CH>(part, pq, lane);
       }
+      // ---- the lane's row: scalar recurrence over the chunk ----
+      float z[CH], zc[CH];  // z[s] = decayed u_s; zc = z at the commit row
+      float cdec = 1.f, ccom = 1.f;
+      int ncom = 0;  // terms of the commit combination (0: commit row not in this chunk)
+#pragma unroll
+      for (int x = 0; x < CH; ++x) z[x] = zc[x] = 0.f;
+#pragma unroll
+      for (int t = 0; t < CH; ++t) {
+        if (t < nc) {
+          const float2 ab = *reinterpret_cast<const float2*>(sSC + 4 * (c0 + t));  // exp(g), beta
+          cdec = __fmul_rn(cdec, ab.x);
+          float r = __fmul_rn(cdec, pk[t]);
+#pragma unroll
+          for (int x = 0; x < CH; ++x)
+            if (x < t) {
+              z[x] = __fmul_rn(z[x], ab.x);
+              r = __fmaf_rn(z[x], sGH[((c0 + x) * R + (c0 + t)) * 2], r);
+            }
+          z[t] = __fmul_rn(ab.y, __fsub_rn(sV[(c0 + t) * DVS + rl], r));
+          if constexpr (kWantO) {
+            float oo = __fmul_rn(cdec, pq[t]);
+#pragma unroll
+            for (int x = 0; x < CH; ++x)
+              if (x <= t) oo = __fmaf_rn(z[x], sGH[((c0 + x) * R + (c0 + t)) * 2 + 1], oo);
+            if (writer) og[(size_t)(c0 + t) * o_tstride] = oo;
+          }
+          if (kCommits && c0 + t == a) {
+#pragma unroll
+            for (int x = 0; x < CH; ++x) zc[x] = x <= t ? z[x] : 0.f;
+            ccom = cdec;
+            ncom = t + 1;
+          }
+          if (kSnap)
+            combine(c0, t + 1, cdec, z, false,
+                    p.snapS + (((size_t)b * R + c0 + t) * p.H_v * p.slices + hs) * DVS * DK);
+        }
+      }
+      // ---- commit: S_a = C_a S0 + sum_{s<=a} z_s k_s^T ----
+      if (kCommits && ncom > 0) {
+        if (last) {
+          combine(c0, ncom, ccom, zc, true, nullptr);
+          store_state(Sg);
+        } else {
+          combine(c0, ncom, ccom, zc, false, Sg);
+        }
+      }
+      // ---- advance the state to the chunk's end when rows follow ----
+      if (!last) combine(c0, nc, cdec, z, true, nullptr);
     }
   }
   pdl_trigger();  // the next call's prologue may launch once every CTA is here
@@ -745,14 +873,18 @@ int check_shape(const gdn_args* a) {
   return GDN_OK;
 }
 
-// Work buffer: wqk [B][H_qk][R][2 d_k], wv [B][R-major v rows per slice], wsc [B][H_v][R][4].
-size_t work_floats(const gdn_args* a, size_t* off_v, size_t* off_sc) {
+// Work buffer: wqk [B][H_qk][R][2 d_k], wv [B][H_v d_v / dvs][R][dvs],
+// wsc [B][H_v][R][4], wgh [B][H_qk][gram_floats(R)].  Every region and every
+// run a rows-kernel item copies is a multiple of 16 bytes.
+size_t work_floats(const gdn_args* a, size_t* off_v, size_t* off_sc, size_t* off_gh) {
   const size_t rows = (size_t)a->B * a->R;
   const size_t qk = rows * a->H_qk * 2 * a->d_k;
   const size_t v = rows * a->H_v * a->d_v;
+  const size_t sc = rows * a->H_v * 4;
   if (off_v) *off_v = qk;
   if (off_sc) *off_sc = qk + v;
-  return qk + v + rows * a->H_v * 4;
+  if (off_gh) *off_gh = qk + v + sc;
+  return qk + v + sc + (size_t)a->B * a->H_qk * gram_floats(a->R);
 }
 
 int validate(const gdn_args* a, unsigned need, Params* out) {
@@ -810,11 +942,12 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.snapS = a->scratch_S;
   p.snapCs = a->scratch_cs;
   p.dvs = rows_per_cta(a->d_k);
-  size_t off_v = 0, off_sc = 0;
-  work_floats(a, &off_v, &off_sc);
+  size_t off_v = 0, off_sc = 0, off_gh = 0;
+  work_floats(a, &off_v, &off_sc, &off_gh);
   p.wqk = static_cast<float*>(a->work);
   p.wv = p.wqk ? p.wqk + off_v : nullptr;
   p.wsc = p.wqk ? p.wqk + off_sc : nullptr;
+  p.wgh = p.wqk ? p.wqk + off_gh : nullptr;
   p.status = a->status;
   return GDN_OK;
 }
@@ -844,7 +977,7 @@ extern "C" {
 
 GDN_API size_t gdn_work_bytes(const gdn_args* args) {
   if (check_shape(args) != GDN_OK) return 0;
-  return sizeof(float) * work_floats(args, nullptr, nullptr);
+  return sizeof(float) * work_floats(args, nullptr, nullptr, nullptr);
 }
 
 GDN_API int gdn_verify(const gdn_args* args, int mode, void* stream) {

@@ -134,7 +134,7 @@ def test_empty_batch_is_a_no_op(cuda_lib):
 def test_work_bytes(cuda_lib):
     a = good_args(cuda_lib)
     B, R, Hq, Hv, dk, dv = 2, 4, 16, 32, 128, 128
-    assert cuda_lib.work_bytes(a) == 4 * B * R * (2 * Hq * dk + Hv * dv + 4 * Hv)
+    assert cuda_lib.work_bytes(a) == 4 * (B * R * (2 * Hq * dk + Hv * dv + 4 * Hv) + B * Hq * ((2 * R * R + 3) // 4 * 4))
     assert cuda_lib.work_bytes(good_args(cuda_lib, d_k=96)) == 0
     assert cuda_lib._lib.gdn_work_bytes(None) == 0
 
