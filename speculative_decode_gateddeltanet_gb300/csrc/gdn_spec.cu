@@ -784,6 +784,24 @@ int launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, c
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
+// Both kernels ask for the same (largest) shared-memory carveout: an SM whose
+// carveout differs from a waiting kernel's cannot take that kernel's CTAs until
+// it drains, which would keep the rows kernel from starting while the
+// prologue still runs.
+template <typename Kernel>
+int prefer_max_shared(Kernel kernel) {
+  static int set_on = -1;  // device on which the preference was last set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (set_on != dev) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+      return GDN_ERR_LAUNCH;
+    set_on = dev;
+  }
+  return GDN_OK;
+}
+
 // Persistent grid of the rows kernel: as many CTAs as fit at once (at most one
 // per item).
 template <int DK, int MODE>
@@ -799,6 +817,7 @@ int launch_rows(const Params& p, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
   if (cache.dev != dev || cache.smem != smem) {
+    if (prefer_max_shared(rows_kernel<DK, MODE>) != GDN_OK) return GDN_ERR_LAUNCH;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(rows_kernel<DK, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
@@ -830,12 +849,18 @@ int dispatch_rows(const Params& p, cudaStream_t st) {
   }
 }
 
+template <typename T, int MODE, int RMAX>
+int launch_prep_r(const Params& p, cudaStream_t st) {
+  const dim3 grid(p.H_qk + (p.H_v * p.d_v + kPrepThreads - 1) / kPrepThreads, p.B), block(kPrepThreads);
+  const int rc = prefer_max_shared(prep_kernel<T, MODE, RMAX>);
+  return rc != GDN_OK ? rc : launch(prep_kernel<T, MODE, RMAX>, grid, block, 0, st, p);
+}
+
 template <typename T, int MODE>
 int launch_prep(const Params& p, cudaStream_t st) {
-  const dim3 grid(p.H_qk + (p.H_v * p.d_v + kPrepThreads - 1) / kPrepThreads, p.B), block(kPrepThreads);
-  if (p.R <= 4) return launch(prep_kernel<T, MODE, 4>, grid, block, 0, st, p);
-  if (p.R <= 8) return launch(prep_kernel<T, MODE, 8>, grid, block, 0, st, p);
-  return launch(prep_kernel<T, MODE, kMaxR>, grid, block, 0, st, p);
+  if (p.R <= 4) return launch_prep_r<T, MODE, 4>(p, st);
+  if (p.R <= 8) return launch_prep_r<T, MODE, 8>(p, st);
+  return launch_prep_r<T, MODE, kMaxR>(p, st);
 }
 
 template <int MODE>
