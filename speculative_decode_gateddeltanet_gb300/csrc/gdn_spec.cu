@@ -130,7 +130,9 @@ __device__ __forceinline__ float tof<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float tof<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-__device__ __forceinline__ float silu(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, expf(-z))); }
+// SiLU with the fast exponential and division (a few ulp; the conv output feeds
+// a normalisation and a dot product, far below the path's tolerance).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, __fadd_rn(1.0f, __expf(-z))); }
 
 __device__ __forceinline__ void flag(int* status, int bit) {
   if (status) atomicOr(status, bit);
@@ -227,7 +229,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   pdl_wait();     // whatever ran before on the stream is complete and visible
   pdl_trigger();  // the rows kernel may start loading its state
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
-  __shared__ float sf[RMAX][2];             // q/k blocks: fq, fk per row
 
   const int b = blockIdx.y;
   int slot, a, report;
@@ -311,46 +312,42 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   }
   if (!qk_block) return;
   __syncthreads();
-  // per-row L2 norms of q and k, one warp per row
-  for (int t = warp; t < t_end; t += kPrepThreads / 32) {
-    float sq = 0.f, sk = 0.f;
-    for (int e = lane; e < DK; e += 32) {
-      const float qv = sy[t][e], kv = sy[t][DK + e];
-      sq = __fmaf_rn(qv, qv, sq);
-      sk = __fmaf_rn(kv, kv, sk);
+  // Raw dot products of the rows' conv outputs in one pass, one warp per entry:
+  // e < n: q_t.q_t;  then pairs (s, t): k_s.k_t (even) and k_s.q_t (odd).
+  // They give the L2 norms (diagonals) and, scaled, the Gram tables.
+  __shared__ float sdot[RMAX + 2 * RMAX * RMAX];
+  const int n = t_end;
+  for (int e = warp; e < n + 2 * n * n; e += kPrepThreads / 32) {
+    const float* x0;
+    const float* x1;
+    if (e < n) {
+      x0 = x1 = &sy[e][0];
+    } else {
+      const int e2 = e - n, which = e2 & 1, s0 = (e2 >> 1) / n, t0 = (e2 >> 1) % n;
+      x0 = &sy[s0][DK];
+      x1 = which ? &sy[t0][0] : &sy[t0][DK];
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      sq = __fadd_rn(sq, __shfl_xor_sync(kFull, sq, off));
-      sk = __fadd_rn(sk, __shfl_xor_sync(kFull, sk, off));
-    }
-    if (lane == 0) {
-      const float fq = __fmul_rn(p.scale, rsqrtf(__fadd_rn(sq, p.eps)));
-      const float fk = rsqrtf(__fadd_rn(sk, p.eps));
-      sf[t][0] = fq;
-      sf[t][1] = fk;
-    }
-  }
-  __syncthreads();
-  if (active) {  // normalise in place and publish scale*q^ | k^
-    float* dst = p.wqk + ((size_t)b * p.H_qk + hq) * p.R * 2 * DK + tid;
-    for (int t = 0; t < t_end; ++t) {
-      const float y = __fmul_rn(sy[t][tid], sf[t][tid < DK ? 0 : 1]);
-      sy[t][tid] = y;
-      dst[(size_t)t * 2 * DK] = y;
-    }
-  }
-  __syncthreads();
-  // Gram tables of the rows: k^_s . k^_t and k^_s . (scale q^_t), one warp per entry
-  float* gh = p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(p.R);
-  for (int e = warp; e < 2 * p.R * p.R; e += kPrepThreads / 32) {
-    const int which = e & 1, st = e >> 1, s0 = st / p.R, t0 = st % p.R;
     float acc = 0.f;
-    if (s0 < t_end && t0 < t_end)
-      for (int j = lane; j < DK; j += 32) acc = __fmaf_rn(sy[s0][DK + j], sy[t0][which ? j : DK + j], acc);
+    for (int j = lane; j < DK; j += 32) acc = __fmaf_rn(x0[j], x1[j], acc);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
-    if (lane == 0) gh[e] = acc;
+    if (lane == 0) sdot[e] = acc;
+  }
+  __syncthreads();
+  auto fq = [&](int t) { return __fmul_rn(p.scale, rsqrtf(__fadd_rn(sdot[t], p.eps))); };
+  auto fk = [&](int t) { return rsqrtf(__fadd_rn(sdot[n + 2 * (t * n + t)], p.eps)); };
+  if (active) {  // publish scale*q^ | k^
+    float* dst = p.wqk + ((size_t)b * p.H_qk + hq) * p.R * 2 * DK + tid;
+    for (int t = 0; t < n; ++t) dst[(size_t)t * 2 * DK] = __fmul_rn(sy[t][tid], tid < DK ? fq(t) : fk(t));
+  }
+  // Gram tables [R][R][2]: k^_s . k^_t and k^_s . (scale q^_t); rows past n are zero
+  float* gh = p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(p.R);
+  for (int i = tid; i < 2 * p.R * p.R; i += kPrepThreads) {
+    const int which = i & 1, s0 = (i >> 1) / p.R, t0 = (i >> 1) % p.R;
+    float val = 0.f;
+    if (s0 < n && t0 < n)
+      val = __fmul_rn(__fmul_rn(sdot[n + 2 * (s0 * n + t0) + which], fk(s0)), which ? fq(t0) : fk(t0));
+    gh[i] = val;
   }
   // per-row decay and write strength of the value heads that read this q/k head
   for (int i = tid; i < p.G * t_end; i += kPrepThreads) {
