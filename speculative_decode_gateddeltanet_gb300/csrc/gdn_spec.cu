@@ -312,26 +312,81 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   }
   if (!qk_block) return;
   __syncthreads();
-  // Raw dot products of the rows' conv outputs in one pass, one warp per entry:
-  // e < n: q_t.q_t;  then pairs (s, t): k_s.k_t (even) and k_s.q_t (odd).
-  // They give the L2 norms (diagonals) and, scaled, the Gram tables.
-  __shared__ float sdot[RMAX + 2 * RMAX * RMAX];
+  // Raw dot products of the rows' conv outputs, packed in n-row order: entries
+  // e < n are q_t.q_t, then pairs (s, t) at n + 2 (s n + t) + {0: k_s.k_t,
+  // 1: k_s.q_t}.  They give the L2 norms (diagonals) and, scaled, the Gram
+  // tables.
   const int n = t_end;
-  for (int e = warp; e < n + 2 * n * n; e += kPrepThreads / 32) {
-    const float* x0;
-    const float* x1;
-    if (e < n) {
-      x0 = x1 = &sy[e][0];
-    } else {
-      const int e2 = e - n, which = e2 & 1, s0 = (e2 >> 1) / n, t0 = (e2 >> 1) % n;
-      x0 = &sy[s0][DK];
-      x1 = which ? &sy[t0][0] : &sy[t0][DK];
-    }
-    float acc = 0.f;
-    for (int j = lane; j < DK; j += 32) acc = __fmaf_rn(x0[j], x1[j], acc);
+  const int nd = n + 2 * n * n;
+  __shared__ float sdot[RMAX + 2 * RMAX * RMAX];
+  if constexpr (RMAX <= 4) {
+    // few rows: thread c < d_k forms all products of its channel, summed by a
+    // warp butterfly and then over the warps' partials in order
+    constexpr int ND = RMAX + 2 * RMAX * RMAX;
+    __shared__ float spart[kPrepThreads / 32][ND];
+    float prod[ND];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
-    if (lane == 0) sdot[e] = acc;
+    for (int e = 0; e < ND; ++e) prod[e] = 0.f;
+    if (tid < DK) {
+      float qv[RMAX], kv[RMAX];
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t) {
+        qv[t] = t < n ? sy[t][tid] : 0.f;
+        kv[t] = t < n ? sy[t][DK + tid] : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t) prod[t] = __fmul_rn(qv[t], qv[t]);
+#pragma unroll
+      for (int s0 = 0; s0 < RMAX; ++s0)
+#pragma unroll
+        for (int t0 = 0; t0 < RMAX; ++t0) {
+          prod[RMAX + 2 * (s0 * RMAX + t0)] = __fmul_rn(kv[s0], kv[t0]);
+          prod[RMAX + 2 * (s0 * RMAX + t0) + 1] = __fmul_rn(kv[s0], qv[t0]);
+        }
+    }
+    if (warp * 32 < DK) {
+#pragma unroll
+      for (int e = 0; e < ND; ++e) {
+        float v = prod[e];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+        prod[e] = v;
+      }
+      if (lane == 0)
+#pragma unroll
+        for (int e = 0; e < ND; ++e) spart[warp][e] = prod[e];
+    }
+    __syncthreads();
+    if (tid < nd) {
+      int src;
+      if (tid < n) {
+        src = tid;
+      } else {
+        const int e2 = tid - n, s0 = (e2 >> 1) / n, t0 = (e2 >> 1) % n;
+        src = RMAX + 2 * (s0 * RMAX + t0) + (e2 & 1);
+      }
+      float acc = 0.f;
+      for (int w = 0; w * 32 < DK; ++w) acc = __fadd_rn(acc, spart[w][src]);
+      sdot[tid] = acc;
+    }
+  } else {
+    // many rows: one warp per entry
+    for (int e = warp; e < nd; e += kPrepThreads / 32) {
+      const float* x0;
+      const float* x1;
+      if (e < n) {
+        x0 = x1 = &sy[e][0];
+      } else {
+        const int e2 = e - n, which = e2 & 1, s0 = (e2 >> 1) / n, t0 = (e2 >> 1) % n;
+        x0 = &sy[s0][DK];
+        x1 = which ? &sy[t0][0] : &sy[t0][DK];
+      }
+      float acc = 0.f;
+      for (int j = lane; j < DK; j += 32) acc = __fmaf_rn(x0[j], x1[j], acc);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
+      if (lane == 0) sdot[e] = acc;
+    }
   }
   __syncthreads();
   auto fq = [&](int t) { return __fmul_rn(p.scale, rsqrtf(__fadd_rn(sdot[t], p.eps))); };
