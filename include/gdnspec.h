@@ -86,7 +86,9 @@ enum {
   GDN_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size  */
   GDN_ERR_UNSUPPORTED = 2, /* W, d_k, d_v, R or dtype outside the set above */
   GDN_ERR_MISALIGNED = 3,  /* a pointer below its required alignment        */
-  GDN_ERR_LAUNCH = 4       /* the CUDA launch failed                        */
+  GDN_ERR_LAUNCH = 4,      /* the CUDA launch failed                        */
+  GDN_ERR_TOO_LARGE = 5    /* the call needs more scratch than the fixed
+                              array of gdn_verify_commit_static holds       */
 };
 
 enum {
@@ -149,6 +151,26 @@ GDN_API int gdn_commit(const gdn_args* args, int mode, void* stream);
  * row and, at row accept_len[b], the slot.  Each state byte is read once and
  * written once.  Needs everything gdn_verify needs plus accept_len. */
 GDN_API int gdn_verify_commit(const gdn_args* args, void* stream);
+
+/* Fused verify + commit that allocates nothing and takes no work buffer
+ * (args->work is ignored and may be NULL).  For callers that cannot hand the
+ * library device memory of their own: code that runs while a CUDA graph is
+ * being captured (cudaMalloc is not a capturable operation), engines that
+ * size every device buffer once at start-up and forbid allocation on the
+ * decode path, and C hosts with no device allocator.  The call's scratch
+ * lives instead in one file-scope device array of GDN_STATIC_WORK_BYTES,
+ * which every GPU that loads this library holds until the process exits.
+ * The first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture starts.
+ * Calls whose scratch (gdn_work_bytes) exceeds the array return
+ * GDN_ERR_TOO_LARGE without launching.  All calls on a device share the one
+ * array, so calls that overlap on the GPU (different streams, or different
+ * host threads without ordering) race on it; the array's contents carry over
+ * from call to call and nothing in it needs to start at zero.  Results equal
+ * gdn_verify_commit's.  The pages have no counterpart: this entry point is a
+ * property of this library's interface, not of the method. */
+#define GDN_STATIC_WORK_BYTES ((size_t)32 << 20)
+GDN_API int gdn_verify_commit_static(const gdn_args* args, void* stream);
 
 /* Bytes of `work` a verify, replay commit or fused call with these shapes
  * needs: 4 * (B * R * (2 * H_qk * d_k + H_v * d_v + 4 * H_v) + B * H_qk * G2), with

@@ -1096,9 +1096,42 @@ GDN_API const char* gdn_strerror(int code) {
              "the int32 and g/beta arrays 4)";
     case GDN_ERR_LAUNCH:
       return "CUDA kernel launch failed";
+    case GDN_ERR_TOO_LARGE:
+      return "the call's scratch exceeds GDN_STATIC_WORK_BYTES (use gdn_verify_commit with a work buffer)";
     default:
       return "unknown gdnspec error code";
   }
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Fused verify + commit without a caller-provided work buffer: the scratch is
+// a file-scope device array.  Host code must not use the array's name as a
+// device address (on the host it names a stand-in object); its device address
+// is looked up once per device with cudaGetSymbolAddress while that device is
+// current, cached, and passed to the kernels like any work buffer.
+#include <atomic>
+
+namespace gdnspec {
+static __device__ __align__(256) unsigned char g_static_work[GDN_STATIC_WORK_BYTES];
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_static_work_addr[kMaxDevices];  // per device, set by its first call
+}  // namespace gdnspec
+
+extern "C" GDN_API int gdn_verify_commit_static(const gdn_args* args, void* stream) {
+  const int rc = check_shape(args);
+  if (rc != GDN_OK) return rc;
+  if (sizeof(float) * work_floats(args, nullptr, nullptr, nullptr) > GDN_STATIC_WORK_BYTES) return GDN_ERR_TOO_LARGE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  void* work = g_static_work_addr[dev].load(std::memory_order_acquire);
+  if (work == nullptr) {
+    if (cudaGetSymbolAddress(&work, g_static_work) != cudaSuccess || work == nullptr) return GDN_ERR_LAUNCH;
+    g_static_work_addr[dev].store(work, std::memory_order_release);
+  }
+  gdn_args a = *args;
+  a.work = work;
+  return gdn_verify_commit(&a, stream);
+}

@@ -13,7 +13,8 @@ import torch
 
 LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libgdnspec.so"
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
+STATIC_WORK_BYTES = 32 << 20
 STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT = 1, 2, 4
 BF16, F32 = 0, 1
 REPLAY, SNAPSHOT = 0, 1
@@ -47,6 +48,8 @@ _lib = ctypes.CDLL(str(LIB_PATH))
 _lib.gdn_verify.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int, _P]
 _lib.gdn_commit.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int, _P]
 _lib.gdn_verify_commit.argtypes = [ctypes.POINTER(GdnArgs), _P]
+_lib.gdn_verify_commit_static.argtypes = [ctypes.POINTER(GdnArgs), _P]
+_lib.gdn_verify_commit_static.restype = ctypes.c_int
 for _f in (_lib.gdn_verify, _lib.gdn_commit, _lib.gdn_verify_commit):
     _f.restype = ctypes.c_int
 _lib.gdn_work_bytes.argtypes = [ctypes.POINTER(GdnArgs)]
@@ -87,6 +90,13 @@ def gdn_commit(args: GdnArgs, mode: int = REPLAY, stream=None) -> None:
 
 def gdn_verify_commit(args: GdnArgs, stream=None) -> None:
     _check(_lib.gdn_verify_commit(ctypes.byref(args), _stream(stream)), "gdn_verify_commit")
+
+
+def gdn_verify_commit_static(args: GdnArgs, stream=None) -> None:
+    """gdn_verify_commit without a work buffer (args.work is ignored): the
+    library's fixed device array of STATIC_WORK_BYTES is the scratch.  For
+    callers that cannot allocate device memory; see include/gdnspec.h."""
+    _check(_lib.gdn_verify_commit_static(ctypes.byref(args), _stream(stream)), "gdn_verify_commit_static")
 
 
 def _ptr(t) -> int | None:

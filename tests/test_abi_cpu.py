@@ -21,7 +21,7 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_work_bytes",
-                                      "gdn_strerror"}
+                                      "gdn_strerror", "gdn_verify_commit_static"}
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):
@@ -52,7 +52,7 @@ def test_struct_layout_matches_header(cuda_lib, tmp_path):
 
 
 def test_strerror_covers_codes(cuda_lib):
-    for code in range(5):
+    for code in range(6):
         assert cuda_lib.strerror(code) and "unknown" not in cuda_lib.strerror(code)
     assert "unknown" in cuda_lib.strerror(99)
 

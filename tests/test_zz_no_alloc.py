@@ -1,0 +1,59 @@
+"""The allocation-free fused entry point, for callers that cannot give the
+library device memory of their own (code running during CUDA graph capture,
+engines that size all device buffers once at start-up, C hosts with no device
+allocator).  It must produce what the regular fused entry point produces, call
+after call, with its scratch in the library's fixed device array; and it must
+refuse, before launching anything, a call whose scratch does not fit."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from gpu_util import O_TOL, S_TOL, bits, valid_rows
+from speculative_decode_gateddeltanet_gb300.inputs import LayerSpec, make_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def test_static_scratch_matches_the_regular_entry_point_on_two_calls():
+    from speculative_decode_gateddeltanet_gb300 import gdn
+
+    spec = LayerSpec("no-alloc-qwen35-B16-k3", B=16, k=3, H_qk=16, H_v=32, d_k=128, d_v=128,
+                     accept="uniform", pool="double")
+    layer = make_layer(spec, 31)
+    regular = gdn.DeviceLayer(layer, "cuda")
+    static = gdn.DeviceLayer(layer, "cuda")
+    valid = torch.from_numpy(valid_rows(layer)).cuda()
+    for _ in range(2):  # the second call starts from the first call's committed slots
+        gdn.gdn_verify_commit(regular.args())
+        a = static.args()
+        a.work = None  # the static entry point takes no work buffer
+        gdn.gdn_verify_commit_static(a)
+        torch.cuda.synchronize()
+        err = (static.o[valid] - regular.o[valid]).abs().max() / regular.o[valid].abs().max()
+        assert float(err) <= O_TOL
+        for s in range(spec.pool_slots):
+            d = torch.linalg.norm(static.ssm_state[s] - regular.ssm_state[s])
+            assert float(d) <= S_TOL * float(torch.linalg.norm(regular.ssm_state[s]))
+        assert torch.equal(bits(static.conv_state), bits(regular.conv_state))
+        assert int(static.status.item()) == 0
+        static.o.fill_(float("nan"))
+        regular.o.fill_(float("nan"))
+
+
+def test_static_scratch_refuses_calls_that_do_not_fit():
+    from speculative_decode_gateddeltanet_gb300 import gdn
+
+    spec = LayerSpec("too-large", B=1024, k=15, H_qk=16, H_v=64, d_k=128, d_v=128)
+    a = gdn.GdnArgs(B=spec.B, R=spec.R, H_qk=spec.H_qk, H_v=spec.H_v, d_k=128, d_v=128, W=4,
+                    pool_slots=spec.B, in_dtype=gdn.BF16, scale=128 ** -0.5, l2_eps=1e-6, flags=0)
+    assert gdn.work_bytes(a) > gdn.STATIC_WORK_BYTES
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_verify_commit_static(a)
+    assert e.value.code == gdn.ERR_TOO_LARGE
