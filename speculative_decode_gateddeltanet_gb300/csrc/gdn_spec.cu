@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "gdnspec.h"
@@ -57,7 +58,10 @@ constexpr unsigned kFull = 0xffffffffu;
 enum Mode : int { kFused = 0, kVerify = 1, kVerifySnap = 2, kCommitReplay = 3 };
 
 struct Params {
-  int B, R, H_qk, H_v, d_k, d_v, P, G, slices;  // slices: d_v / DVS items per value head
+  int B, R, H_qk, H_v, d_k, d_v, P, G;
+  int nw;      // warps per CTA
+  int dvs;     // state rows per item: nw * ROWS_W
+  int slices;  // items per value head: d_v / dvs
   long long C;
   float scale, eps;
   const void* x;
@@ -79,7 +83,9 @@ struct Params {
   int* status;
 };
 
-// Lane geometry of the rows kernel for a d_k-column state.
+// Lane geometry of the state rows for a d_k-column state.  A warp holds
+// ROWS_W rows; a CTA has nw (1..8, chosen per call) warps, so an item is a
+// slice of DVS = nw * ROWS_W state rows.
 template <int DK>
 struct Geo {
   static constexpr int LPR = DK >= 32 ? 8 : 4;   // lanes per state row
@@ -87,11 +93,9 @@ struct Geo {
   static constexpr int RG = 32 / LPR;            // row groups per warp
   static constexpr int M = DK >= 64 ? 4 : 2;     // rows per lane
   static constexpr int ROWS_W = RG * M;          // rows per warp
-  static constexpr int NW = DK == 16 ? 1 : (M == 4 ? 2 : 4);  // warps per CTA
-  static constexpr int DVS = NW * ROWS_W;        // state rows per CTA (32, or 16 at d_k = 16)
-  static constexpr int NT = NW * 32;
-  static constexpr int MIN_CTAS = NT == 64 ? 8 : (NT == 128 ? 5 : 16);  // resident CTAs per SM the registers must allow
 };
+constexpr int kMaxWarps = 8;
+constexpr int kMaxThreads = 32 * kMaxWarps;
 
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 // Floats of one (request, q/k head) Gram table [R][R][2], padded to 16 bytes so
@@ -249,8 +253,7 @@ __device__ __forceinline__ int request_rows_of(const Params& p, int n, int slot,
 // region starts on 16 bytes), then two input stages of stage_bytes() each.
 template <int DK>
 struct Layout {
-  static constexpr int DVS = Geo<DK>::DVS;
-  int R, qs, ipc, es;
+  int R, qs, ipc, es, DVS;
   __host__ __device__ int nd4() const { return (R + 2 * R * R + 3) & ~3; }
   __host__ __device__ int qk() const { return DVS * DK; }                 // [R][2 DK]       scale*q^ | k^
   __host__ __device__ int v() const { return qk() + R * 2 * DK; }         // [IPC][R][DVS]   v
@@ -286,9 +289,20 @@ __device__ __forceinline__ int cluster_total() {
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return (int)r;
 }
-// arrive releases this thread's shared-memory writes to the cluster; wait
-// acquires every thread's writes released by the arrivals it waited for
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+// Arrive publishing this thread's earlier shared-memory writes to the cluster.
+// The fence is restricted to shared memory, so global stores still in flight
+// (committed state, o, windows) are not waited for, as a plain release would.
+__device__ __forceinline__ void cluster_arrive_shared() {
+  asm volatile(
+      "fence.release.sync_restrict::shared::cta.cluster;\n\t"
+      "barrier.cluster.arrive.relaxed.aligned;" ::
+          : "memory");
+}
+// Arrive with no ordering: the thread's reads of its peers have completed.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+// Wait for every thread of the cluster to arrive; acquires what they published.
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // the address of the same shared-memory location in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer(const void* ptr, int rank) {
@@ -298,20 +312,22 @@ __device__ __forceinline__ uint32_t peer(const void* ptr, int rank) {
 }
 __device__ __forceinline__ float ld_peer(uint32_t addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ float4 ld_peer4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
-// ---- 4-byte asynchronous copies global -> shared, completed per thread by group ----
+// ---- asynchronous copies global -> shared (4 or 16 bytes), completed per thread by group ----
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // all but the newest `N` committed groups of this thread have landed
@@ -368,10 +384,11 @@ __device__ __forceinline__ int lane_of_row(int m) {
 }
 
 template <int DK, typename T, int MODE>
-__global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(const Params p) {
+__global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const Params p) {
   using Gm = Geo<DK>;
   constexpr int LPR = Gm::LPR, NC4 = Gm::NC4, RG = Gm::RG, M = Gm::M;
-  constexpr int DVS = Gm::DVS, ROWS_W = Gm::ROWS_W, NT = Gm::NT;
+  constexpr int ROWS_W = Gm::ROWS_W;
+  const int NT = blockDim.x, DVS = p.dvs;
   constexpr int NP = 2 * NC4;  // column pairs per lane per row
   constexpr int CH = 4;        // rows per chunk
   constexpr int kDup = (LPR >> ilog2(M)) - 1;  // low lane bits that repeat a row's sums
@@ -379,13 +396,13 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
   constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
   constexpr bool kReplay = MODE == kCommitReplay;
   constexpr bool kSnap = MODE == kVerifySnap;
-  constexpr uint32_t kSBytes = DVS * DK * sizeof(float);
+  const uint32_t kSBytes = DVS * DK * sizeof(float);
   constexpr int ES = sizeof(T);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = p.R, qs = p.qs, ipc = p.ipc, cs = p.cs;
   const int nqk = 2 * qs, nv = ipc * DVS;
-  const Layout<DK> L{R, qs, ipc, ES};
+  const Layout<DK> L{R, qs, ipc, ES, DVS};
   extern __shared__ __align__(16) float smem[];
   float* const stS = smem;  // [DVS][DK] state slice of the next item
   float* const sQK = smem + L.qk();
@@ -397,80 +414,91 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
   float* const sDot = smem + L.dot();
   unsigned char* const stage0 = reinterpret_cast<unsigned char*>(smem + L.stage());
   auto stage = [&](int s) { return stage0 + s * L.stage_bytes(); };
-  __shared__ __align__(8) uint64_t barS, barIn[2];
-  __shared__ int sMeta[2][3];  // per group parity: slot, rows to run, commit row (-1 none)
-  // producer (thread 0) state, kept out of the registers every thread holds:
-  // meta of the current and next group, request data of group k + 2, phases
-  // requested on barS, barIn[0], barIn[1]
-  __shared__ int sProd[3][3], sReq[3], sIssued[3];
+  __shared__ __align__(8) uint64_t barS;
+  __shared__ int sMeta[3][3];  // group k's at [k % 3]: slot, rows to run, commit row (-1 none)
+  __shared__ int sReq[3];      // request data of group k + 2, loaded by thread 0 at group k's start
+  __shared__ int sIssued, sCons;  // state copies requested; consumed when a wait gave up
 
   // cluster coordinates are re-read where they are used rather than kept live
   // through the row recurrence
   const int K = cluster_index() < p.n_groups ? (p.n_groups - 1 - cluster_index()) / cluster_total() + 1 : 0;
 
-  // ---- producer side (thread 0) ----
-  struct Meta {
-    int slot, rows, crow;
-  };
-  struct Req {
-    int n, slot, a;
-  };
-  auto load_req = [&](int gi) {
+  auto load_req = [&](int gi) {  // thread 0
     const int b = gi / p.H_qk;
-    Req q;
-    q.n = p.n_rows[b];
-    q.slot = p.slot_ids[b];
-    q.a = kCommits ? p.accept_len[b] : 0;
-    return q;
+    sReq[0] = p.n_rows[b];
+    sReq[1] = p.slot_ids[b];
+    sReq[2] = kCommits ? p.accept_len[b] : 0;
   };
-  auto eval_req = [&](int gi, const Req& q) {
-    const int hq = gi % p.H_qk, rank = cluster_rank();
-    Meta m;
+  // thread 0: request data (n, slot, a) -> sMeta[k % 3]; reports a bad request once
+  auto eval_req = [&](int k, int n, int slot, int a) {
+    const int gi = cluster_index() + k * cluster_total();
+    int* m = sMeta[k % 3];
     int report = 0;
-    m.slot = q.slot;
-    m.rows = request_rows_of<kCommits, kReplay>(p, q.n, q.slot, q.a, m.crow, report);
-    if (report && hq == 0 && rank == 0) flag(p.status, report);
-    return m;
+    m[0] = slot;
+    m[1] = request_rows_of<kCommits, kReplay>(p, n, slot, a, m[2], report);
+    if (report && gi % p.H_qk == 0 && cluster_rank() == 0) flag(p.status, report);
   };
-  auto issue_inputs = [&](int s, int gi, const Meta& m) {
-    if (m.rows == 0) {
-      mbar_arrive(&barIn[s]);
-      return;
-    }
-    const int b = gi / p.H_qk, hq = gi - b * p.H_qk, rank = cluster_rank();
-    const T* X = static_cast<const T*>(p.x);
+  // first channels of this CTA's q share, k share and v channels in group gi
+  auto share = [&](int gi, long long& chq, long long& chk, long long& chv) {
+    const int hq = gi % p.H_qk, rank = cluster_rank();
+    chq = (long long)hq * DK + (long long)rank * qs;
+    chk = (long long)p.H_qk * DK + chq;
+    chv = 2LL * p.H_qk * DK + (long long)hq * p.G * p.d_v + (long long)rank * nv;
+  };
+  // a run of 16-byte chunks, chunk c issued by thread (base + c) % NT (NT a power of two)
+  auto copy_run = [&](unsigned char* dst, const T* src, int bytes, int& base) {
+    const int n = bytes >> 4;
+    for (int c = (tid - base) & (NT - 1); c < n; c += NT)
+      cp_async16(dst + 16 * c, reinterpret_cast<const unsigned char*>(src) + 16 * c);
+    base += n;
+  };
+  // x rows and taps of group k into stage k & 1 (no request data needed: every row of x exists)
+  auto issue_x = [&](int k) {
+    const int gi = cluster_index() + k * cluster_total(), b = gi / p.H_qk;
+    long long chq, chk, chv;
+    share(gi, chq, chk, chv);
+    const int bq = qs * ES, bv = nv * ES;
+    const T* X = static_cast<const T*>(p.x) + (size_t)b * R * p.C;
     const T* Wt = static_cast<const T*>(p.conv_w);
-    const T* CS = static_cast<const T*>(p.conv_state);
-    const long long chq = (long long)hq * DK + (long long)rank * qs;
-    const long long chk = (long long)p.H_qk * DK + chq;
-    const long long chv = 2LL * p.H_qk * DK + (long long)hq * p.G * p.d_v + (long long)rank * nv;
-    const uint32_t bq = qs * ES, bv = nv * ES;
-    mbar_expect_tx(&barIn[s], m.rows * (2 * bq + bv) + 2 * bq * (kW + kWS) + bv * (kW + kWS));
-    unsigned char* st = stage(s);
-    for (int t = 0; t < m.rows; ++t) {
-      const T* xr = X + ((size_t)b * R + t) * p.C;
-      bulk_load(st + t * 2 * bq, xr + chq, bq, &barIn[s]);
-      bulk_load(st + t * 2 * bq + bq, xr + chk, bq, &barIn[s]);
-      bulk_load(st + L.st_xv() + t * bv, xr + chv, bv, &barIn[s]);
+    unsigned char* st = stage(k & 1);
+    int base = 0;
+    for (int t = 0; t < R; ++t) {
+      copy_run(st + t * 2 * bq, X + t * p.C + chq, bq, base);
+      copy_run(st + t * 2 * bq + bq, X + t * p.C + chk, bq, base);
+      copy_run(st + L.st_xv() + t * bv, X + t * p.C + chv, bv, base);
     }
-    const T* csr = CS + (size_t)m.slot * p.C * kWS;
-    bulk_load(st + L.st_w(), Wt + chq * kW, kW * bq, &barIn[s]);
-    bulk_load(st + L.st_w() + kW * bq, Wt + chk * kW, kW * bq, &barIn[s]);
-    bulk_load(st + L.st_cs(), csr + chq * kWS, kWS * bq, &barIn[s]);
-    bulk_load(st + L.st_cs() + kWS * bq, csr + chk * kWS, kWS * bq, &barIn[s]);
-    bulk_load(st + L.st_wv(), Wt + chv * kW, kW * bv, &barIn[s]);
-    bulk_load(st + L.st_csv(), csr + chv * kWS, kWS * bv, &barIn[s]);
+    copy_run(st + L.st_w(), Wt + chq * kW, kW * bq, base);
+    copy_run(st + L.st_w() + kW * bq, Wt + chk * kW, kW * bq, base);
+    copy_run(st + L.st_wv(), Wt + chv * kW, kW * bv, base);
   };
-  auto issue_state = [&](int gi, int i, const Meta& m) {
-    if (m.rows == 0) {
+  // committed conv windows of group k (after its request data: none for a request that runs no rows)
+  auto issue_cs = [&](int k) {
+    const int* m = sMeta[k % 3];
+    if (m[1] == 0) return;
+    long long chq, chk, chv;
+    share(cluster_index() + k * cluster_total(), chq, chk, chv);
+    const int bq = qs * ES, bv = nv * ES;
+    const T* csr = static_cast<const T*>(p.conv_state) + (size_t)m[0] * p.C * kWS;
+    unsigned char* st = stage(k & 1);
+    int base = 0;
+    copy_run(st + L.st_cs(), csr + chq * kWS, kWS * bq, base);
+    copy_run(st + L.st_cs() + kWS * bq, csr + chk * kWS, kWS * bq, base);
+    copy_run(st + L.st_csv(), csr + chv * kWS, kWS * bv, base);
+  };
+  // thread 0: item i of group k's state slice into the state buffer (one bulk copy)
+  auto issue_state = [&](int k, int i) {
+    const int* m = sMeta[k % 3];
+    ++sIssued;
+    if (m[1] == 0) {
       mbar_arrive(&barS);
       return;
     }
+    const int gi = cluster_index() + k * cluster_total();
     const int hs = (gi % p.H_qk) * p.G * p.slices + cluster_rank() * ipc + i;  // h * slices + sl
     mbar_expect_tx(&barS, kSBytes);
-    bulk_load(stS, p.S + ((size_t)m.slot * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS);
+    bulk_load(stS, p.S + ((size_t)m[0] * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS);
   };
-  // decay and write strength rows of the CTA's items in group k, into buffer k & 1
+  // decay and write strength rows of the CTA's items in group k, into buffer k & 1; commits
   auto issue_ab = [&](int k) {
     if (k < K) {
       const int gi = cluster_index() + k * cluster_total(), rank = cluster_rank();
@@ -485,43 +513,48 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
     cp_async_commit();
   };
 
-  auto put_meta = [&](int* dst, const Meta& m) {
-    dst[0] = m.slot;
-    dst[1] = m.rows;
-    dst[2] = m.crow;
-  };
-  auto get_meta = [&](const int* src) { return Meta{src[0], src[1], src[2]}; };
+  // Copies in flight per thread, as commit groups: {x 0, ab 0}, {x 1}, {cs 0, cs 1},
+  // then per group k: {ab k+1} at its start and {x k+2, cs k+2} after its prologue.
+  // At group k's start that leaves group k's inputs behind at most 1 (k = 0) or
+  // 2 newer groups.
   if (tid == 0) {
-    sIssued[0] = sIssued[1] = sIssued[2] = 0;
+    sIssued = 0;
     mbar_init(&barS, 1);
-    mbar_init(&barIn[0], 1);
-    mbar_init(&barIn[1], 1);
   }
   pdl_wait();     // whatever ran before on the stream is complete and visible
   pdl_trigger();  // the next call may launch; it waits for this grid before reading
-  __syncthreads();  // the barriers are initialised before anyone waits on them
-  issue_ab(0);
+  // Start-up: the first two groups' request data (both loads in flight at
+  // once), their x rows and taps meanwhile, then their windows, and only
+  // then the first state slice, so the small loads are not queued behind it.
+  int q0[3] = {0, 0, 0}, q1[3] = {0, 0, 0};
   if (tid == 0) {
     const int cid = cluster_index(), ncl = cluster_total();
-    Req q0{}, q1{};
-    if (K > 0) q0 = load_req(cid);
-    if (K > 1) q1 = load_req(cid + ncl);
     if (K > 0) {
-      const Meta m = eval_req(cid, q0);
-      put_meta(sMeta[0], m);
-      put_meta(sProd[0], m);
-      issue_inputs(0, cid, m);
-      issue_state(cid, 0, m);
-      sIssued[0] = sIssued[1] = 1;
+      const int b = cid / p.H_qk;
+      q0[0] = p.n_rows[b];
+      q0[1] = p.slot_ids[b];
+      q0[2] = kCommits ? p.accept_len[b] : 0;
     }
     if (K > 1) {
-      const Meta m = eval_req(cid + ncl, q1);
-      put_meta(sMeta[1], m);
-      put_meta(sProd[1], m);
-      issue_inputs(1, cid + ncl, m);
-      sIssued[2] = 1;
+      const int b = (cid + ncl) / p.H_qk;
+      q1[0] = p.n_rows[b];
+      q1[1] = p.slot_ids[b];
+      q1[2] = kCommits ? p.accept_len[b] : 0;
     }
   }
+  if (K > 0) issue_x(0);
+  issue_ab(0);
+  if (K > 1) issue_x(1);
+  cp_async_commit();
+  if (tid == 0) {
+    if (K > 0) eval_req(0, q0[0], q0[1], q0[2]);
+    if (K > 1) eval_req(1, q1[0], q1[1], q1[2]);
+  }
+  __syncthreads();  // the barrier is initialised and the first groups' request data published
+  if (K > 0) issue_cs(0);
+  if (K > 1) issue_cs(1);
+  cp_async_commit();
+  if (tid == 0 && K > 0) issue_state(0, 0);
 
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
@@ -531,35 +564,24 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
   const bool writer = (lane & kDup) == 0;
   const size_t o_tstride = (size_t)p.H_v * p.d_v;
 
-  // A wait that gives up sets `broken`: the CTA records where (sCons: phases
-  // consumed on barS, barIn[0], barIn[1]), stops computing and requesting
-  // copies, but keeps taking part in the cluster's barriers.
-  __shared__ int sCons[3];
+  // A wait that gives up sets `broken`: the CTA records how many state copies it
+  // consumed, stops computing and requesting state, but keeps taking part in
+  // the cluster's barriers.
   bool broken = false;
   for (int k = 0; k < K; ++k) {
     const int s = k & 1;
     const int gi = cluster_index() + k * cluster_total();
     const int b = gi / p.H_qk, hq = gi - b * p.H_qk;
-    if (tid == 0 && k + 2 < K) {  // producer: request data of group k + 2, in flight during the prologue
-      const Req q = load_req(gi + 2 * cluster_total());
-      sReq[0] = q.n;
-      sReq[1] = q.slot;
-      sReq[2] = q.a;
-    }
-    __syncthreads();  // the previous group's items are done with the tables and sV
-    issue_ab(k + 1);  // buffer (k+1)&1 was last read by group k-1's items
-    if (!broken && __syncthreads_or(!mbar_wait(&barIn[s], (k >> 1) & 1))) {
-      broken = true;
-      if (tid == 0) {
-        flag(p.status, GDN_STATUS_TIMEOUT);
-        sCons[0] = k * ipc;
-        sCons[1] = (k + 1) >> 1;
-        sCons[2] = k >> 1;
-      }
-    }
-    const int slot = sMeta[s][0], rows = broken ? 0 : sMeta[s][1], crow = sMeta[s][2];
-    cp_async_wait<1>();  // this thread's decay/strength copies of group k have landed
+    if (tid == 0 && k + 2 < K) load_req(gi + 2 * cluster_total());  // in flight during the prologue
+    __syncthreads();  // the previous group's items are done with the tables, sV and sAB
+    issue_ab(k + 1);
+    if (k == 0)
+      cp_async_wait<1>();  // this thread's copies of group k have landed
+    else
+      cp_async_wait<2>();
     if (k > 0) cluster_wait();  // every peer has finished reading this CTA's sY and sPD
+    __syncthreads();            // every thread's copies of group k are visible
+    const int slot = sMeta[k % 3][0], rows = sMeta[k % 3][1], crow = sMeta[k % 3][2];
 
     // ---- conv + SiLU of the CTA's channels; committed or per-row windows ----
     if (rows > 0) {
@@ -608,7 +630,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
             c2 = r2;
           }
         }
-        if (kCommits && crow >= 0) {  // this thread is the channel's only reader in the call
+        if (kCommits && crow >= 0 && !broken) {  // this thread is the channel's only reader in the call
           T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
           cs[0] = c0;
           cs[1] = c1;
@@ -622,29 +644,44 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
     // 1: k_s.q_t}; and exp(g) of the decay rows ----
     const int n = rows, nd = n + 2 * n * n;
     if (rows > 0) {
-      for (int e = tid; e < nd; e += NT) {
-        const float* x0;
-        const float* x1;
-        if (e < n) {
-          x0 = x1 = sY + e * nqk;
-        } else {
-          const int e2 = e - n, which = e2 & 1, s0 = (e2 >> 1) / n, t0 = (e2 >> 1) % n;
-          x0 = sY + s0 * nqk + qs;
-          x1 = sY + t0 * nqk + (which ? 0 : qs);
-        }
+      // each entry over 4 adjacent lanes (quarters of the share, joined by two
+      // shuffles in a fixed order); the trip count is the same for every lane
+      const int nq = qs >> 2, quarter = tid & 3;
+      for (int e0 = 0; e0 < nd; e0 += NT >> 2) {
+        const int e = e0 + (tid >> 2);
         float acc = 0.f;
-        for (int j = 0; j < qs; ++j) acc = __fmaf_rn(x0[j], x1[j], acc);
-        sPD[e] = acc;
+        if (e < nd) {
+          const float* x0;
+          const float* x1;
+          if (e < n) {
+            x0 = x1 = sY + e * nqk;
+          } else {
+            const int e2 = e - n, which = e2 & 1, s0 = (e2 >> 1) / n, t0 = (e2 >> 1) % n;
+            x0 = sY + s0 * nqk + qs;
+            x1 = sY + t0 * nqk + (which ? 0 : qs);
+          }
+          x0 += quarter * nq;
+          x1 += quarter * nq;
+          for (int j = 0; j < nq; ++j) acc = __fmaf_rn(x0[j], x1[j], acc);
+        }
+        acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, 1));
+        acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, 2));
+        if (e < nd && quarter == 0) sPD[e] = acc;
       }
       float* ab = sABall + s * 2 * ipc * R;
       for (int j = tid; j < ipc * R; j += NT) ab[2 * j] = expf(ab[2 * j]);
     }
-    cluster_arrive();  // the partials and the conv output of every CTA are published
+    cluster_arrive_shared();  // the partials and the conv output of every CTA are published
     cluster_wait();
     if (rows > 0) {
       for (int e = tid; e < nd; e += NT) {
+        float v[8];  // every peer's partial in flight at once, then summed in rank order
+#pragma unroll
+        for (int r = 0; r < 8; ++r) v[r] = r < cs ? ld_peer(peer(sPD + e, r)) : 0.f;
         float acc = 0.f;
-        for (int r = 0; r < cs; ++r) acc = __fadd_rn(acc, ld_peer(peer(sPD + e, r)));
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < cs) acc = __fadd_rn(acc, v[r]);
         sDot[e] = acc;
       }
     }
@@ -662,28 +699,40 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
       }
       // every share's rows, scaled: scale*q^ | k^
       constexpr int kChunks = 2 * DK / 4;
-      for (int j = tid; j < n * kChunks; j += NT) {
-        const int t = j / kChunks, cc = (j - t * kChunks) * 4;
-        const bool isk = cc >= DK;
-        const int cq = isk ? cc - DK : cc;
-        const int r = cq / qs, off = cq - r * qs + (isk ? qs : 0);
-        const float4 v = ld_peer4(peer(sY + t * nqk + off, r));
-        const float f = isk ? fk(t) : fq(t);
-        *reinterpret_cast<float4*>(sQK + t * 2 * DK + cc) =
-            make_float4(__fmul_rn(v.x, f), __fmul_rn(v.y, f), __fmul_rn(v.z, f), __fmul_rn(v.w, f));
+      constexpr int kBatch = 4;  // remote loads in flight per thread
+      for (int j0 = tid; j0 < n * kChunks; j0 += kBatch * NT) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u * NT;
+          if (j < n * kChunks) {
+            const int t = j / kChunks, cc = (j - t * kChunks) * 4;
+            const bool isk = cc >= DK;
+            const int cq = isk ? cc - DK : cc;
+            const int r = cq / qs, off = cq - r * qs + (isk ? qs : 0);
+            v[u] = ld_peer4(peer(sY + t * nqk + off, r));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u * NT;
+          if (j < n * kChunks) {
+            const int t = j / kChunks, cc = (j - t * kChunks) * 4;
+            const float f = cc >= DK ? fk(t) : fq(t);
+            *reinterpret_cast<float4*>(sQK + t * 2 * DK + cc) =
+                make_float4(__fmul_rn(v[u].x, f), __fmul_rn(v[u].y, f), __fmul_rn(v[u].z, f), __fmul_rn(v[u].w, f));
+          }
+        }
       }
     }
-    cluster_arrive();  // this CTA has read what it needs from its peers; waited on at the next group
-    __syncthreads();  // tables complete; stage s consumed
-    if (tid == 0 && !broken && k + 2 < K) {  // stage s is free: inputs of group k + 2
-      fence_proxy_async();
-      const int g2 = gi + 2 * cluster_total();
-      const Meta m = eval_req(g2, Req{sReq[0], sReq[1], sReq[2]});
-      put_meta(sMeta[s], m);
-      put_meta(sProd[(k + 2) % 3], m);
-      issue_inputs(s, g2, m);
-      ++sIssued[1 + s];
+    cluster_arrive_relaxed();  // this CTA has read what it needs from its peers; waited on at the next group
+    if (tid == 0 && k + 2 < K) eval_req(k + 2, sReq[0], sReq[1], sReq[2]);
+    __syncthreads();  // tables complete; stage s consumed; group k + 2's request data published
+    if (k + 2 < K) {
+      issue_x(k + 2);
+      issue_cs(k + 2);
     }
+    cp_async_commit();
 
     // ---- the CTA's items ----
     for (int i = 0; i < ipc; ++i) {
@@ -691,9 +740,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
         broken = true;
         if (tid == 0) {
           flag(p.status, GDN_STATUS_TIMEOUT);
-          sCons[0] = k * ipc + i;
-          sCons[1] = (k + 2) >> 1;
-          sCons[2] = (k + 1) >> 1;
+          sCons = k * ipc + i;
         }
       }
       const bool run = rows > 0 && !broken;
@@ -712,12 +759,10 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
       if (tid == 0 && !broken) {
         if (i + 1 < ipc) {
           fence_proxy_async();
-          issue_state(gi, i + 1, get_meta(sProd[k % 3]));
-          ++sIssued[0];
+          issue_state(k, i + 1);
         } else if (k + 1 < K) {
           fence_proxy_async();
-          issue_state(gi + cluster_total(), 0, get_meta(sProd[(k + 1) % 3]));
-          ++sIssued[0];
+          issue_state(k + 1, 0);
         }
       }
       if (!run) continue;
@@ -898,9 +943,8 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) verify_kernel(
   }
   if (K > 0) cluster_wait();  // no peer reads this CTA's shared memory after it exits
   cp_async_wait<0>();
-  if (broken && tid == 0)  // let copies still in flight land before leaving (bounded)
-    for (int j = 0; j < 3; ++j)
-      for (int ph = sCons[j]; ph < sIssued[j]; ++ph) mbar_wait(j == 0 ? &barS : &barIn[j - 1], ph & 1);
+  if (broken && tid == 0)  // let a state copy still in flight land before leaving (bounded)
+    for (int ph = sCons; ph < sIssued; ++ph) mbar_wait(&barS, ph & 1);
 }
 
 // Snapshot commit: slot <- scratch row accept_len[b] (state and conv window).
@@ -957,12 +1001,11 @@ int prefer_max_shared(Kernel kernel) {
 // Persistent grid: as many clusters as fit at once (at most one per group).
 template <int DK, typename T, int MODE>
 int launch_verify(const Params& p, cudaStream_t st) {
-  using Gm = Geo<DK>;
   auto kernel = verify_kernel<DK, T, MODE>;
-  const size_t smem = Layout<DK>{p.R, p.qs, p.ipc, (int)sizeof(T)}.bytes();
+  const size_t smem = Layout<DK>{p.R, p.qs, p.ipc, (int)sizeof(T), p.dvs}.bytes();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.cs);
-  cfg.blockDim = dim3(Gm::NT);
+  cfg.blockDim = dim3(32 * p.nw);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -977,13 +1020,13 @@ int launch_verify(const Params& p, cudaStream_t st) {
   struct Cache {
     int dev = -1;
     size_t smem = 0;
-    int cs = 0;
+    int cs = 0, nw = 0;
     int clusters = 0;  // resident clusters on the device for this shape
   };
   static Cache cache;  // per instantiation
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
-  if (cache.dev != dev || cache.smem != smem || cache.cs != p.cs) {
+  if (cache.dev != dev || cache.smem != smem || cache.cs != p.cs || cache.nw != p.nw) {
     if (prefer_max_shared(kernel) != GDN_OK) return GDN_ERR_LAUNCH;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -993,6 +1036,7 @@ int launch_verify(const Params& p, cudaStream_t st) {
     cache.dev = dev;
     cache.smem = smem;
     cache.cs = p.cs;
+    cache.nw = p.nw;
     cache.clusters = n;
   }
   const int ncl = p.n_groups < cache.clusters ? p.n_groups : cache.clusters;
@@ -1022,7 +1066,11 @@ int run_mode(const Params& p, int in_dtype, cudaStream_t st) {
 
 inline bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-inline int rows_per_cta(int d_k) { return d_k >= 32 ? Geo<32>::DVS : Geo<16>::DVS; }
+// d_v must be a multiple of this (two warps of state rows at the smallest d_k)
+inline int d_v_unit(int d_k) { return d_k >= 32 ? 32 : 16; }
+inline int rows_per_warp(int d_k) {
+  return d_k >= 64 ? Geo<64>::ROWS_W : (d_k == 32 ? Geo<32>::ROWS_W : Geo<16>::ROWS_W);
+}
 
 // Cluster shape of a call: CS CTAs per (request, q/k head) group, each taking
 // QS = d_k / CS q (and k) channels and IPC = G * slices / CS state items.  CS
@@ -1034,24 +1082,57 @@ inline int cluster_size(int d_k, int items, int es) {
   return 1;
 }
 
-// Dynamic shared memory of one CTA for a call's shape (0 if d_k is not built).
-inline size_t kernel_smem(int d_k, int R, int G, int d_v, int es) {
-  const int slices = d_v / rows_per_cta(d_k);
-  const int cs = cluster_size(d_k, G * slices, es), qs = d_k / cs, ipc = G * slices / cs;
+// Dynamic shared memory of one CTA (0 if d_k is not built).
+inline size_t layout_bytes(int d_k, int R, int qs, int ipc, int es, int dvs) {
   switch (d_k) {
     case 16:
-      return Layout<16>{R, qs, ipc, es}.bytes();
+      return Layout<16>{R, qs, ipc, es, dvs}.bytes();
     case 32:
-      return Layout<32>{R, qs, ipc, es}.bytes();
+      return Layout<32>{R, qs, ipc, es, dvs}.bytes();
     case 64:
-      return Layout<64>{R, qs, ipc, es}.bytes();
+      return Layout<64>{R, qs, ipc, es, dvs}.bytes();
     case 128:
-      return Layout<128>{R, qs, ipc, es}.bytes();
+      return Layout<128>{R, qs, ipc, es, dvs}.bytes();
     default:
       return 0;
   }
 }
 constexpr size_t kMaxSmem = 227 * 1024;  // opt-in shared memory per block on sm_103
+
+struct Plan {
+  int nw, dvs, slices, cs, qs, ipc;
+};
+// Item and cluster shape of a call.  Warps per CTA: the most (8, 4, 2, 1) whose
+// slice of state rows divides d_v and whose CTA fits in shared memory while
+// the call still has at least one item per SM; a call with fewer items than
+// SMs takes the fewest warps (the most, smallest items).  False if no shape fits.
+inline bool plan_call(const gdn_args* a, int sms, Plan* out) {
+  const int es = a->in_dtype == GDN_DTYPE_BF16 ? 2 : 4;
+  const int G = a->H_v / a->H_qk, rw = rows_per_warp(a->d_k);
+  bool have_best = false, have_any = false;
+  Plan best{}, last{};
+  for (int nw = kMaxWarps; nw >= 1; nw >>= 1) {
+    Plan q;
+    q.nw = nw;
+    q.dvs = nw * rw;
+    if (a->d_v % q.dvs != 0) continue;
+    q.slices = a->d_v / q.dvs;
+    q.cs = cluster_size(a->d_k, G * q.slices, es);
+    q.qs = a->d_k / q.cs;
+    q.ipc = G * q.slices / q.cs;
+    const size_t smem = layout_bytes(a->d_k, a->R, q.qs, q.ipc, es, q.dvs);
+    if (smem == 0 || smem > kMaxSmem) continue;
+    last = q;
+    have_any = true;
+    if (!have_best && (long long)a->B * a->H_v * q.slices >= sms) {
+      best = q;
+      have_best = true;
+    }
+  }
+  if (!have_any) return false;
+  *out = have_best ? best : last;
+  return true;
+}
 
 enum Need : unsigned {
   kNeedRows = 1u,  // x, g, beta, conv_w, work
@@ -1069,12 +1150,12 @@ int check_shape(const gdn_args* a) {
   if (a->in_dtype != GDN_DTYPE_BF16 && a->in_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
   if (a->W != kW || a->R > kMaxR) return GDN_ERR_UNSUPPORTED;
   if (a->d_k != 16 && a->d_k != 32 && a->d_k != 64 && a->d_k != 128) return GDN_ERR_UNSUPPORTED;
-  if (a->d_v % rows_per_cta(a->d_k) != 0) return GDN_ERR_UNSUPPORTED;
+  if (a->d_v % d_v_unit(a->d_k) != 0) return GDN_ERR_UNSUPPORTED;
   if (a->H_v % a->H_qk != 0) return GDN_ERR_UNSUPPORTED;
   if (a->B > 65535) return GDN_ERR_UNSUPPORTED;
   if ((long long)a->H_v * a->d_v > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
-  if (kernel_smem(a->d_k, a->R, a->H_v / a->H_qk, a->d_v, a->in_dtype == GDN_DTYPE_BF16 ? 2 : 4) > kMaxSmem)
-    return GDN_ERR_UNSUPPORTED;
+  Plan plan;
+  if (!plan_call(a, 1, &plan)) return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
 }
 
@@ -1130,7 +1211,6 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.d_v = a->d_v;
   p.P = a->pool_slots;
   p.G = a->H_v / a->H_qk;
-  p.slices = a->d_v / rows_per_cta(a->d_k);
   p.C = 2LL * a->H_qk * a->d_k + (long long)a->H_v * a->d_v;
   p.scale = a->scale;
   p.eps = a->l2_eps;
@@ -1146,19 +1226,38 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.o = a->o;
   p.snapS = a->scratch_S;
   p.snapCs = a->scratch_cs;
-  const int es = a->in_dtype == GDN_DTYPE_BF16 ? 2 : 4;
-  p.cs = cluster_size(a->d_k, p.G * p.slices, es);
-  p.qs = a->d_k / p.cs;
-  p.ipc = p.G * p.slices / p.cs;
   p.n_groups = a->B * a->H_qk;
   p.status = a->status;
   return GDN_OK;
+}
+
+// SMs of the current device (cached per device; 0 on error).
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 int run_rows(const gdn_args* args, unsigned need, int mode, void* stream) {
   Params p;
   const int rc = validate(args, need, &p);
   if (rc != GDN_OK || p.B == 0) return rc;
+  const int sms = sm_count();
+  Plan plan;
+  if (sms == 0) return GDN_ERR_LAUNCH;
+  if (!plan_call(args, sms, &plan)) return GDN_ERR_UNSUPPORTED;
+  p.nw = plan.nw;
+  p.dvs = plan.dvs;
+  p.slices = plan.slices;
+  p.cs = plan.cs;
+  p.qs = plan.qs;
+  p.ipc = plan.ipc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (mode) {
     case kFused:
@@ -1237,7 +1336,6 @@ GDN_API const char* gdn_strerror(int code) {
 // device address (on the host it names a stand-in object); its device address
 // is looked up once per device with cudaGetSymbolAddress while that device is
 // current, cached, and passed to the kernels like any work buffer.
-#include <atomic>
 
 namespace gdnspec {
 static __device__ __align__(256) unsigned char g_static_work[GDN_STATIC_WORK_BYTES];

@@ -1,9 +1,9 @@
-"""Alignment of every bulk async copy the kernel issues, for every supported
-head size, input dtype, row count and group shape: a copy must start and end
-on a 16-byte boundary on both the shared and the global side.  The formulas
-mirror csrc/gdn_spec.cu's `Layout`, `cluster_size` and the copies of
-`issue_inputs` / `issue_state`; `gdn_work_bytes` is checked through the
-library."""
+"""Alignment of every asynchronous copy the kernel issues, for every supported
+head size, input dtype, row count, group shape and CTA size: a copy must start
+and end on a 16-byte boundary on both the shared and the global side.  The
+formulas mirror csrc/gdn_spec.cu's `Layout`, `cluster_size` and the copies of
+`issue_x` / `issue_cs` / `issue_state`; `gdn_work_bytes` is checked through
+the library."""
 from __future__ import annotations
 
 import itertools
@@ -18,7 +18,11 @@ def gram_floats(R):
     return (2 * R * R + 3) & ~3
 
 
-def dvs(dk):
+def rows_per_warp(dk):
+    return 8 if dk == 32 else 16
+
+
+def dv_unit(dk):
     return 16 if dk == 16 else 32
 
 
@@ -32,8 +36,7 @@ def cluster_size(dk, items, es):
 class Layout:
     """Shared-memory layout of one CTA (float offsets, then two byte stages)."""
 
-    def __init__(self, dk, R, qs, ipc, es):
-        D = dvs(dk)
+    def __init__(self, dk, R, qs, ipc, es, D):
         nd4 = (R + 2 * R * R + 3) & ~3
         self.qk = D * dk
         self.v = self.qk + R * 2 * dk
@@ -52,13 +55,16 @@ class Layout:
         self.bytes = 4 * self.stage + 2 * self.stage_bytes
 
 
-SHAPES = list(itertools.product([16, 32, 64, 128], [2, 4], [1, 2, 3, 4, 8], [1, 2, 3, 4]))
+SHAPES = list(itertools.product([16, 32, 64, 128], [2, 4], [1, 2, 3, 4, 8], [1, 2, 3, 4], [1, 2, 4, 8]))
 
 
-@pytest.mark.parametrize("dk,es,slices,G", SHAPES)
-def test_every_bulk_copy_is_16_byte_aligned(dk, es, slices, G):
-    D = dvs(dk)
-    dv = slices * D
+@pytest.mark.parametrize("dk,es,units,G,nw", SHAPES)
+def test_every_copy_is_16_byte_aligned(dk, es, units, G, nw):
+    dv = units * dv_unit(dk)
+    D = nw * rows_per_warp(dk)
+    if dv % D:
+        pytest.skip("slice does not divide d_v")
+    slices = dv // D
     items = G * slices
     cs = cluster_size(dk, items, es)
     qs, ipc = dk // cs, items // cs
@@ -67,7 +73,7 @@ def test_every_bulk_copy_is_16_byte_aligned(dk, es, slices, G):
         Hv = Hq * G
         C = 2 * Hq * dk + Hv * dv
         for R in range(1, 17):
-            L = Layout(dk, R, qs, ipc, es)
+            L = Layout(dk, R, qs, ipc, es, D)
             if L.bytes > MAX_SMEM:
                 continue  # rejected by the library's shape check
             # shared side: every region and stage piece starts on 16 bytes
@@ -101,15 +107,17 @@ def test_every_bulk_copy_is_16_byte_aligned(dk, es, slices, G):
 
 
 def test_cluster_shape_of_the_qwen_layer():
-    # 16 q/k heads of 128, 32 value heads of 128: 8 items per group, 8 CTAs
-    assert cluster_size(128, 2 * 4, 2) == 8
-    L = Layout(128, 4, 16, 1, 2)
-    assert L.bytes * 8 <= 228 * 1024  # eight CTAs of one cluster fit on one SM
+    # 16 q/k heads of 128, 32 value heads of 128, 8 warps (a whole head) per CTA:
+    # 2 items per group, clusters of 2 CTAs with 64 q and 64 k channels each
+    D = 8 * rows_per_warp(128)
+    assert D == 128 and cluster_size(128, 2 * (128 // D), 2) == 2
+    L = Layout(128, 4, 64, 1, 2, D)
+    assert 2 * (L.bytes + 1024) <= 228 * 1024  # two CTAs fit on one SM
 
 
 @pytest.mark.parametrize("dk,B,R,Hq,G", list(itertools.product([16, 128], [1, 3], [1, 3, 9, 16], [1, 2], [1, 4])))
 def test_work_bytes_formula(cuda_lib, dk, B, R, Hq, G):
-    Hv, dv = Hq * G, dvs(dk) * 2
+    Hv, dv = Hq * G, dv_unit(dk) * 2
     total = B * R * Hq * 2 * dk + B * R * Hv * dv + B * R * Hv * 4 + B * Hq * gram_floats(R)
     a = cuda_lib.GdnArgs(B=B, R=R, H_qk=Hq, H_v=Hv, d_k=dk, d_v=dv, W=4, pool_slots=1,
                          in_dtype=cuda_lib.BF16, scale=1.0, l2_eps=1e-6, flags=0)
@@ -118,7 +126,11 @@ def test_work_bytes_formula(cuda_lib, dk, B, R, Hq, G):
 
 def test_oversized_shared_memory_is_rejected(cuda_lib):
     # 128 value heads of 256 on one q/k head: 128 items per CTA do not fit
-    assert Layout(128, 16, 16, 128, 2).bytes > MAX_SMEM
+    for nw in (1, 2, 4, 8):
+        D = nw * rows_per_warp(128)
+        items = 128 * (256 // D)
+        cs = cluster_size(128, items, 2)
+        assert Layout(128, 16, 128 // cs, items // cs, 2, D).bytes > MAX_SMEM
     a = cuda_lib.GdnArgs(B=1, R=16, H_qk=1, H_v=128, d_k=128, d_v=256, W=4, pool_slots=1,
                          in_dtype=cuda_lib.BF16, scale=1.0, l2_eps=1e-6, flags=0)
     assert cuda_lib.work_bytes(a) == 0
