@@ -186,16 +186,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
-// Validity of request b as every kernel reads it.  Returns the number of rows
-// to run (0 = nothing to do for this request); `report` receives a status bit
-// for a bad request (the caller decides who records it).
+// Validity of a request as every kernel reads it, from its n_rows n, slot and
+// accept length a.  Returns the number of rows to run (0 = nothing to do for
+// this request); crow receives the commit row (-1: none) and `report` a status
+// bit for a bad request (the caller decides who records it).
 template <bool kCommits, bool kReplay>
-__device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, int& a, bool& commit, int& report) {
+__device__ __forceinline__ int request_rows_of(const Params& p, int n, int slot, int a, int& crow, int& report) {
   report = 0;
-  commit = false;
-  a = -1;
-  const int n = p.n_rows[b];
-  slot = p.slot_ids[b];
+  crow = -1;
   if (n == 0) return 0;
   if (slot < 0 || slot >= p.P) {
     report = GDN_STATUS_BAD_SLOT;
@@ -206,14 +204,24 @@ __device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, i
     return 0;
   }
   if (kCommits) {
-    a = p.accept_len[b];
-    commit = a >= 0 && a < n;
-    if (!commit) {
+    if (a >= 0 && a < n) {
+      crow = a;
+    } else {
       report = GDN_STATUS_BAD_ACCEPT;
       if (kReplay) return 0;
     }
   }
   return kReplay ? a + 1 : n;
+}
+// The same for request b, read from the call's arrays.
+template <bool kCommits, bool kReplay>
+__device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, int& a, bool& commit, int& report) {
+  slot = p.slot_ids[b];
+  a = kCommits ? p.accept_len[b] : -1;
+  int crow;
+  const int rows = request_rows_of<kCommits, kReplay>(p, p.n_rows[b], slot, a, crow, report);
+  commit = crow >= 0;
+  return rows;
 }
 
 // ------------------------------------------------------------ prologue
@@ -515,14 +523,26 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   __shared__ int sMeta[2][3];  // per item parity: slot, rows to run, commit row (-1 none)
 
   // ---- producer side (thread 0) ----
-  auto meta = [&](int it, int& slot, int& rows, int& commit_row) {
+  // An item's request data is loaded one item ahead of its use and evaluated
+  // only when its copies are issued, so the producer's warp never waits on
+  // those loads while the item before it computes.
+  struct Req {
+    int n, slot, a;
+  };
+  auto load_req = [&](int it) {
     const int b = it / (p.H_v * p.slices);
-    const int hs = it - b * p.H_v * p.slices;
-    int a, report;
-    bool commit;
-    rows = request_rows<kCommits, MODE == kCommitReplay>(p, b, slot, a, commit, report);
+    Req q;
+    q.n = p.n_rows[b];
+    q.slot = p.slot_ids[b];
+    q.a = kCommits ? p.accept_len[b] : -1;
+    return q;
+  };
+  auto meta = [&](int it, const Req& q, int& slot, int& rows, int& commit_row) {
+    const int hs = it % (p.H_v * p.slices);
+    int report;
+    slot = q.slot;
+    rows = request_rows_of<kCommits, MODE == kCommitReplay>(p, q.n, q.slot, q.a, commit_row, report);
     if (report && hs == 0) flag(p.status, report);
-    commit_row = commit ? a : -1;
   };
   auto issue_state = [&](int it, int slot, int rows) {
     if (rows == 0) {
@@ -551,20 +571,21 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
               &barQ[s]);
   };
 
-  int nslot = 0, nrows = 0, ncrow = -1;  // producer: meta of the item after the current one
+  Req qn{0, 0, -1};  // producer: request data of the item after the current one
   if (tid == 0) {
     mbar_init(&barS, 1);
     mbar_init(&barQ[0], 1);
     mbar_init(&barQ[1], 1);
     if (blockIdx.x < n_items) {
+      const Req q0 = load_req(blockIdx.x);
+      if (blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);  // both in flight
       int slot, rows, crow;
-      meta(blockIdx.x, slot, rows, crow);
+      meta(blockIdx.x, q0, slot, rows, crow);
       sMeta[0][0] = slot;
       sMeta[0][1] = rows;
       sMeta[0][2] = crow;
       issue_state(blockIdx.x, slot, rows);  // before the prologue has finished
     }
-    if (blockIdx.x + gridDim.x < n_items) meta(blockIdx.x + gridDim.x, nslot, nrows, ncrow);
   }
   __syncthreads();  // the barriers are initialised before anyone waits on them
   pdl_wait();       // the prologue's q, k, v and tables are complete and visible
@@ -608,12 +629,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       const int it1 = it + gridDim.x;
       if (it1 < n_items) {
         fence_proxy_async();  // the reads above happen before the bulk copies overwrite the buffers
+        int nslot, nrows, ncrow;
+        meta(it1, qn, nslot, nrows, ncrow);  // loaded an item ago
         sMeta[s ^ 1][0] = nslot;
         sMeta[s ^ 1][1] = nrows;
         sMeta[s ^ 1][2] = ncrow;
         issue_state(it1, nslot, nrows);
         issue_rows(s ^ 1, it1, nrows);
-        if (it1 + gridDim.x < n_items) meta(it1 + gridDim.x, nslot, nrows, ncrow);  // in flight meanwhile
+        if (it1 + gridDim.x < n_items) qn = load_req(it1 + gridDim.x);  // in flight while this item computes
       }
     }
     if (rows == 0) continue;
@@ -842,16 +865,10 @@ int launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, c
 // prologue still runs.
 template <typename Kernel>
 int prefer_max_shared(Kernel kernel) {
-  static int set_on = -1;  // device on which the preference was last set
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
-  if (set_on != dev) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-      return GDN_ERR_LAUNCH;
-    set_on = dev;
-  }
-  return GDN_OK;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_LAUNCH;
 }
 
 // Persistent grid of the rows kernel: as many CTAs as fit at once (at most one
@@ -904,8 +921,14 @@ int dispatch_rows(const Params& p, cudaStream_t st) {
 template <typename T, int MODE, int RMAX>
 int launch_prep_r(const Params& p, cudaStream_t st) {
   const dim3 grid(p.H_qk + (p.H_v * p.d_v + kPrepThreads - 1) / kPrepThreads, p.B), block(kPrepThreads);
-  const int rc = prefer_max_shared(prep_kernel<T, MODE, RMAX>);
-  return rc != GDN_OK ? rc : launch(prep_kernel<T, MODE, RMAX>, grid, block, 0, st, p);
+  static int set_on = -1;  // device on which this instantiation's carveout was last set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (set_on != dev) {
+    if (prefer_max_shared(prep_kernel<T, MODE, RMAX>) != GDN_OK) return GDN_ERR_LAUNCH;
+    set_on = dev;
+  }
+  return launch(prep_kernel<T, MODE, RMAX>, grid, block, 0, st, p);
 }
 
 template <typename T, int MODE>
