@@ -272,7 +272,7 @@ def run_cuda(args, rank, ws, local):
         "bytes_per_row": round(bytes_per_step / rows_per_step),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "kernel": "rows_kernel<128,bf16,%s>" % args.mode,
+                     "kernel": "rows_kernel<128, %s>" % args.mode,
                      "traffic": measured_traffic(spec.name, args.mode),
                      "algorithmic_bytes_per_launch": round(per_launch_bytes)},
         "e2e": {"value": round(rows_per_step * ws / (e2e_ms / 1e3), 1), "unit": UNIT,
