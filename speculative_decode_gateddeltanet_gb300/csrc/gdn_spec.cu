@@ -353,16 +353,28 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
         }
     }
     if (warp * 32 < DK) {
+      // entries 0..31: reduce-scatter over the warp (each step a lane keeps
+      // half of its values and adds the partner's copy of that half), so lane
+      // e ends with entry e's sum; the rest: a plain butterfly
+      static_assert(ND >= 32, "the reduce-scatter takes the first 32 entries");
 #pragma unroll
-      for (int e = 0; e < ND; ++e) {
+      for (int off = 16, half = 16; off >= 1; off >>= 1, half >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? prod[i] : prod[i + half];
+          const float keep = up ? prod[i + half] : prod[i];
+          prod[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
+        }
+      }
+      spart[warp][lane] = prod[0];
+#pragma unroll
+      for (int e = 32; e < ND; ++e) {
         float v = prod[e];
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
-        prod[e] = v;
+        if (lane == 0) spart[warp][e] = v;
       }
-      if (lane == 0)
-#pragma unroll
-        for (int e = 0; e < ND; ++e) spart[warp][e] = prod[e];
     }
     __syncthreads();
     if (tid < nd) {
