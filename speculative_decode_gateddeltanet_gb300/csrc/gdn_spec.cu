@@ -583,7 +583,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
               &barQ[s]);
   };
 
+  // Two producer threads, one per warp, so each warp issues part of the next
+  // item's copies: thread 0 the state slice, thread 32 (thread 0 when the CTA
+  // has one warp) the q/k/v rows and tables.  Both keep the next item's
+  // request data.
+  constexpr int kRowsProducer = Gm::NT > 32 ? 32 : 0;
+  const bool producer = tid == 0 || tid == kRowsProducer;
   Req qn{0, 0, -1};  // producer: request data of the item after the current one
+  if (tid == kRowsProducer && blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);
   if (tid == 0) {
     mbar_init(&barS, 1);
     mbar_init(&barQ[0], 1);
@@ -601,7 +608,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   }
   __syncthreads();  // the barriers are initialised before anyone waits on them
   pdl_wait();       // the prologue's q, k, v and tables are complete and visible
-  if (tid == 0 && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1]);
+  if (tid == kRowsProducer && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1]);
 
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
@@ -637,17 +644,19 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         }
     }
     __syncthreads();  // the state buffer is free: request the next item
-    if (tid == 0) {
+    if (producer) {
       const int it1 = it + gridDim.x;
       if (it1 < n_items) {
         fence_proxy_async();  // the reads above happen before the bulk copies overwrite the buffers
         int nslot, nrows, ncrow;
         meta(it1, qn, nslot, nrows, ncrow);  // loaded an item ago
-        sMeta[s ^ 1][0] = nslot;
-        sMeta[s ^ 1][1] = nrows;
-        sMeta[s ^ 1][2] = ncrow;
-        issue_state(it1, nslot, nrows);
-        issue_rows(s ^ 1, it1, nrows);
+        if (tid == 0) {
+          sMeta[s ^ 1][0] = nslot;
+          sMeta[s ^ 1][1] = nrows;
+          sMeta[s ^ 1][2] = ncrow;
+          issue_state(it1, nslot, nrows);
+        }
+        if (tid == kRowsProducer) issue_rows(s ^ 1, it1, nrows);
         if (it1 + gridDim.x < n_items) qn = load_req(it1 + gridDim.x);  // in flight while this item computes
       }
     }
