@@ -191,6 +191,14 @@ def run_cuda(args, rank, ws, local):
                 gdn.gdn_commit(a, m, sp)
 
     launches_per_step = len(cargs) * (1 if args.mode == "fused" else 2)
+    # --graph: the step's launches captured once into a CUDA graph and replayed
+    graph = None
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     rows_per_step = sum(int(h["n_rows"].clamp(min=0).sum()) for h in host)
     bytes_per_step = sum(spec_bytes(h["spec"], h["n_rows"]) for h in host)
 
@@ -198,6 +206,14 @@ def run_cuda(args, rank, ws, local):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                run_step()
+        torch.cuda.synchronize()
 
     # ---- device-resident timed region ----
     sampler = ClockSampler(local) if rank == 0 else None
@@ -209,7 +225,7 @@ def run_cuda(args, rank, ws, local):
     ev0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
-            step()
+            run_step()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -266,6 +282,7 @@ def run_cuda(args, rank, ws, local):
         "config": {"workload": spec.name, "layers": len(cargs), "B": spec.B, "k": spec.k, "rows_per_layer":
                    rows_per_step // len(cargs), "H_qk": spec.H_qk, "H_v": spec.H_v, "d_k": spec.d_k,
                    "d_v": spec.d_v, "storage": "bf16 x/conv, fp32 g/beta/state/o", "mode": args.mode,
+                   "launch": "cuda graph replay" if args.graph else "stream launches",
                    "l2": "inputs larger than L2: each step streams %.2f GB over %d distinct layers"
                          % (bytes_per_step / 1e9, len(cargs))},
         "hbm_gbs": round(bytes_per_step * ws / (ms_step / 1e3) / 1e9, 1),
@@ -353,6 +370,9 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=None, help="requests per layer (default: the workload's 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch each step's kernels on the stream instead of replaying the step captured "
+                         "as a CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
