@@ -27,7 +27,10 @@
  *
  * Layouts (row-major, C = 2*H_qk*d_k + H_v*d_v, channels [q heads|k heads|v heads]):
  *   x           [B][R][C]             in_dtype   pre-conv rows; row t < n_rows[b] valid
- *   g, beta     [B][R][H_v]           fp32       log-decay (exp(g) is the decay), write strength
+ *   g, beta     [B][R][H_v]           fp32       log-decay (exp(g) is the decay), write strength;
+ *                                                with GDN_FLAG_RAW_GATING the raw projections
+ *                                                a and b they are formed from (below)
+ *   A_log       [H_v]                 fp32       GDN_FLAG_RAW_GATING only
  *   conv_w      [C][W]                in_dtype   depthwise taps, tap W-1 multiplies the newest row
  *   conv_state  [pool_slots][C][W-1]  in_dtype   committed window, oldest column first
  *   ssm_state   [pool_slots][H_v][d_v][d_k] fp32 committed state S (d_v x d_k per head)
@@ -99,6 +102,12 @@ enum {
                                 bounded wait: that block wrote nothing                */
 };
 enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
+/* flags: GDN_FLAG_RAW_GATING - g and beta hold a layer's raw gating
+ * projections a and b, and the prologue forms, per row and value head h,
+ *   g = -exp(A_log[h]) * softplus(a),   beta = sigmoid(b)
+ * (the standard gating of a Qwen3.5-style GDN layer; the pages feed the
+ * recurrence these per-head scalars without printing how they are formed). */
+enum { GDN_FLAG_RAW_GATING = 1 };
 enum { GDN_REPLAY = 0, GDN_SNAPSHOT = 1 };
 
 typedef struct gdn_args {
@@ -113,7 +122,7 @@ typedef struct gdn_args {
   int32_t in_dtype;   /* GDN_DTYPE_* of x, conv_w, conv_state, scratch_cs      */
   float scale;        /* o = scale * S q (usually d_k^-1/2), finite            */
   float l2_eps;       /* >= 0, added to sum y^2 before the square root         */
-  int32_t flags;      /* must be 0                                             */
+  int32_t flags;      /* 0 or GDN_FLAG_RAW_GATING                              */
   const void* x;      /* 16-byte aligned: x, conv_w, conv_state, ssm_state, o,  */
   const float* g;     /* scratch_S, scratch_cs; 4-byte: g, beta, int32 arrays   */
   const float* beta;
@@ -128,6 +137,7 @@ typedef struct gdn_args {
   void* scratch_cs;          /* snapshot mode only                             */
   void* work;                /* verify, replay commit and fused calls          */
   int32_t* status;           /* may be NULL                                    */
+  const float* A_log;        /* GDN_FLAG_RAW_GATING only (4-byte aligned)      */
 } gdn_args;
 
 /* Verify: for every active request, run rows 0..n_rows-1 from its slot's

@@ -56,6 +56,8 @@ def _load():
         lib.oracle_gdn_verify_commit.argtypes = [
             ctypes.POINTER(_Dims), dp, dp, dp, dp, dp, dp, ip, ip, ip, dp, dp, dp, ctypes.c_int]
         lib.oracle_gdn_verify_commit.restype = ctypes.c_int
+        lib.oracle_gdn_gating.argtypes = [ctypes.c_long, ctypes.c_int, dp, dp, dp, dp, dp]
+        lib.oracle_gdn_gating.restype = None
         _lib = lib
     return _lib
 
@@ -77,14 +79,30 @@ def _ptr(a, ty):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(ty))
 
 
+def gating(a, b, A_log):
+    """g = -exp(A_log) softplus(a), beta = sigmoid(b) per row and value head
+    (fp64, ``oracle_gdn_gating``); a, b are [..][H_v], A_log is [H_v]."""
+    a64, b64 = _f64(a), _f64(b)
+    shape = a64.shape
+    hv = shape[-1]
+    n = a64.size // hv
+    g = np.empty(shape)
+    beta = np.empty(shape)
+    dp = ctypes.c_double
+    _load().oracle_gdn_gating(n, hv, _ptr(_f64(A_log), dp), _ptr(a64, dp), _ptr(b64, dp),
+                              _ptr(g, dp), _ptr(beta, dp))
+    return g, beta
+
+
 def verify_commit(layer: dict, *, commit: bool = True, snapshot: bool = False,
                   accept_len=None, scale: float | None = None, l2_eps: float = DEFAULT_EPS,
-                  mutation: int | str = 0, requests=None) -> dict:
+                  mutation: int | str = 0, requests=None, raw_gating: bool = False) -> dict:
     """Run the oracle on one layer call (the dict ``inputs.make_layer`` returns).
 
     commit=False is a verify-only call (slots untouched).  ``requests``
     restricts the call to a subset of request indices (for sampled checks at
-    full size); the other requests are treated as inactive.  Returns fp64
+    full size); the other requests are treated as inactive.  raw_gating=True
+    forms g and beta from the layer's raw projections a_raw, b_raw and A_log.  Returns fp64
     numpy arrays: o [B][R][H_v][d_v] (NaN where not produced), the slot pools
     after the call, the status bits, and with snapshot=True the per-row
     states and conv windows."""
@@ -93,6 +111,8 @@ def verify_commit(layer: dict, *, commit: bool = True, snapshot: bool = False,
     dims = _Dims(B, R, spec.H_qk, spec.H_v, spec.d_k, spec.d_v, W, spec.pool_slots,
                  spec.d_k ** -0.5 if scale is None else scale, l2_eps)
     x, g, beta = _f64(layer["x"]), _f64(layer["g"]), _f64(layer["beta"])
+    if raw_gating:  # the layer's raw gating projections instead of g and beta
+        g, beta = gating(layer["a_raw"], layer["b_raw"], layer["A_log"])
     conv_w = _f64(layer["conv_w"])
     conv_state = _f64(layer["conv_state"]).copy()
     ssm_state = _f64(layer["ssm_state"]).copy()

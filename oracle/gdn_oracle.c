@@ -74,6 +74,24 @@ typedef struct {
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* Gating of a Qwen3.5-style GDN layer from its raw projections, per row and
+ * value head h:  g = -exp(A_log[h]) * softplus(a),  beta = sigmoid(b), with
+ * softplus(a) = log(1 + e^a) and sigmoid(b) = 1 / (1 + e^-b), written in the
+ * overflow-free forms max(a, 0) + log1p(e^-|a|) and e^min(b,0) / (1 + e^-|b|).
+ * a, b, g, beta are [n][Hv]; A_log is [Hv].  The pages feed the recurrence
+ * these two per-head scalars without printing how they are formed; this is
+ * the layer's standard recipe (decay always <= 0, strength in (0, 1)). */
+void oracle_gdn_gating(long n, int Hv, const double* A_log, const double* a, const double* b,
+                       double* g, double* beta) {
+  for (long r = 0; r < n; ++r)
+    for (int h = 0; h < Hv; ++h) {
+      const double av = a[r * Hv + h], bv = b[r * Hv + h];
+      const double softplus = (av > 0.0 ? av : 0.0) + log1p(exp(-fabs(av)));
+      g[r * Hv + h] = -exp(A_log[h]) * softplus;
+      beta[r * Hv + h] = exp(bv < 0.0 ? bv : 0.0) / (1.0 + exp(-fabs(bv)));
+    }
+}
+
 /* Verify (and optionally commit) every request, one decode step per row.
  *
  * accept_len == NULL: verify only; conv_state and ssm_state are not written.

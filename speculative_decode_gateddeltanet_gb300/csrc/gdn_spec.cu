@@ -79,6 +79,8 @@ struct Params {
   float* wsc;  // work: [B][H_v][R][4]              exp(g), beta, 0, 0
   float* wgh;  // work: [B][H_qk][gram_floats(R)]   [R][R][2]: k^_s . k^_t, k^_s . (scale q^_t)
   int* status;
+  const float* A_log;  // GDN_FLAG_RAW_GATING: g and beta hold the raw projections a and b
+  int raw_gating;
 };
 
 // Lane geometry of the rows kernel for a d_k-column state.
@@ -432,8 +434,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
       g_i = __ldg(p.g + gi);
       beta_i = __ldg(p.beta + gi);
     }
+    float gg = g_i, bb = beta_i;
+    if (p.raw_gating) {  // g = -exp(A_log) softplus(a), beta = sigmoid(b), overflow-free forms
+      gg = -expf(__ldg(p.A_log + h)) * (fmaxf(g_i, 0.f) + log1pf(expf(-fabsf(g_i))));
+      bb = 1.f / (1.f + expf(-beta_i));
+    }
     *reinterpret_cast<float4*>(p.wsc + (((size_t)b * p.H_v + h) * p.R + t) * 4) =
-        make_float4(expf(g_i), beta_i, 0.f, 0.f);
+        make_float4(expf(gg), bb, 0.f, 0.f);
   }
 }
 
@@ -983,7 +990,7 @@ int check_shape(const gdn_args* a) {
   if (a->B < 0 || a->R < 1 || a->H_qk < 1 || a->H_v < 1 || a->d_k < 1 || a->d_v < 1 || a->W < 1 ||
       a->pool_slots < 1)
     return GDN_ERR_INVALID_ARG;
-  if (a->flags != 0) return GDN_ERR_INVALID_ARG;
+  if ((a->flags & ~GDN_FLAG_RAW_GATING) != 0) return GDN_ERR_INVALID_ARG;
   if (a->in_dtype != GDN_DTYPE_BF16 && a->in_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
   if (a->W != kW || a->R > kMaxR) return GDN_ERR_UNSUPPORTED;
   if (a->d_k != 16 && a->d_k != 32 && a->d_k != 64 && a->d_k != 128) return GDN_ERR_UNSUPPORTED;
@@ -1019,6 +1026,8 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
     return GDN_ERR_MISALIGNED;
   if (need & kNeedRows) {
     if (!a->x || !a->g || !a->beta || !a->conv_w || !a->work) return GDN_ERR_INVALID_ARG;
+    if ((a->flags & GDN_FLAG_RAW_GATING) && !a->A_log) return GDN_ERR_INVALID_ARG;
+    if ((a->flags & GDN_FLAG_RAW_GATING) && !aligned(a->A_log, 4)) return GDN_ERR_MISALIGNED;
     if (!aligned(a->x, 16) || !aligned(a->conv_w, 16) || !aligned(a->g, 4) || !aligned(a->beta, 4) ||
         !aligned(a->work, 16))
       return GDN_ERR_MISALIGNED;
@@ -1070,6 +1079,8 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.wsc = p.wqk ? p.wqk + off_sc : nullptr;
   p.wgh = p.wqk ? p.wqk + off_gh : nullptr;
   p.status = a->status;
+  p.raw_gating = (a->flags & GDN_FLAG_RAW_GATING) != 0;
+  p.A_log = p.raw_gating ? a->A_log : nullptr;
   return GDN_OK;
 }
 

@@ -17,6 +17,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH, ERR_TOO_LARGE 
 STATIC_WORK_BYTES = 32 << 20
 STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT = 1, 2, 4
 BF16, F32 = 0, 1
+FLAG_RAW_GATING = 1
 REPLAY, SNAPSHOT = 0, 1
 
 _I32, _F32, _P = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
@@ -31,7 +32,7 @@ class GdnArgs(ctypes.Structure):
         ("flags", _I32),
         ("x", _P), ("g", _P), ("beta", _P), ("conv_w", _P), ("conv_state", _P), ("ssm_state", _P),
         ("slot_ids", _P), ("n_rows", _P), ("accept_len", _P), ("o", _P), ("scratch_S", _P),
-        ("scratch_cs", _P), ("work", _P), ("status", _P),
+        ("scratch_cs", _P), ("work", _P), ("status", _P), ("A_log", _P),
     ]
 
 
@@ -105,11 +106,13 @@ def _ptr(t) -> int | None:
 
 def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_qk: int,
               accept_len=None, o=None, scratch_S=None, scratch_cs=None, work=None,
-              status=None, scale: float | None = None, l2_eps: float = 1e-6) -> GdnArgs:
+              status=None, scale: float | None = None, l2_eps: float = 1e-6, A_log=None) -> GdnArgs:
     """Fill a GdnArgs from tensors laid out as ``include/gdnspec.h`` states.
 
     Shapes are read from x [B][R][C], ssm_state [P][H_v][d_v][d_k] and
-    conv_w [C][W]; the tensors must stay alive while the call runs."""
+    conv_w [C][W]; the tensors must stay alive while the call runs.  With
+    A_log given, g and beta are the raw gating projections (the raw-gating
+    flag is set)."""
     B, R, _ = x.shape
     P, H_v, d_v, d_k = ssm_state.shape
     W = conv_w.shape[1]
@@ -121,11 +124,12 @@ def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_
         raise TypeError(f"unsupported input dtype {x.dtype}")
     return GdnArgs(
         B=B, R=R, H_qk=H_qk, H_v=H_v, d_k=d_k, d_v=d_v, W=W, pool_slots=P, in_dtype=dt,
-        scale=d_k ** -0.5 if scale is None else scale, l2_eps=l2_eps, flags=0,
+        scale=d_k ** -0.5 if scale is None else scale, l2_eps=l2_eps,
+        flags=0 if A_log is None else FLAG_RAW_GATING,
         x=_ptr(x), g=_ptr(g), beta=_ptr(beta), conv_w=_ptr(conv_w), conv_state=_ptr(conv_state),
         ssm_state=_ptr(ssm_state), slot_ids=_ptr(slot_ids), n_rows=_ptr(n_rows),
         accept_len=_ptr(accept_len), o=_ptr(o), scratch_S=_ptr(scratch_S),
-        scratch_cs=_ptr(scratch_cs), work=_ptr(work), status=_ptr(status))
+        scratch_cs=_ptr(scratch_cs), work=_ptr(work), status=_ptr(status), A_log=_ptr(A_log))
 
 
 class DeviceLayer:
@@ -138,11 +142,16 @@ class DeviceLayer:
     KEYS = ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows", "accept_len")
 
     def __init__(self, layer: dict, device="cuda", snapshot: bool = False, scale=None,
-                 l2_eps: float = 1e-6):
+                 l2_eps: float = 1e-6, raw_gating: bool = False):
         self.spec = layer["spec"]
         s = self.spec
         for k in self.KEYS:
             setattr(self, k, layer[k].to(device).contiguous())
+        self.A_log = None
+        if raw_gating:  # g and beta hold the raw projections; the library forms the gating
+            self.g = layer["a_raw"].to(device).contiguous()
+            self.beta = layer["b_raw"].to(device).contiguous()
+            self.A_log = layer["A_log"].to(device).contiguous()
         self.o = torch.full((s.B, s.R, s.H_v, s.d_v), float("nan"), device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.scratch_S = self.scratch_cs = None
@@ -159,4 +168,4 @@ class DeviceLayer:
                          slot_ids=self.slot_ids, n_rows=self.n_rows, accept_len=self.accept_len,
                          o=self.o, scratch_S=self.scratch_S, scratch_cs=self.scratch_cs,
                          work=self.work, status=self.status, H_qk=self.spec.H_qk,
-                         scale=self.scale, l2_eps=self.l2_eps)
+                         scale=self.scale, l2_eps=self.l2_eps, A_log=self.A_log)

@@ -19,6 +19,8 @@ Shapes (all row-major):
   slot_ids   [B] int32            request -> slot
   n_rows     [B] int32            valid rows (k_b + 1), 0 = inactive request
   accept_len [B] int32            accepted drafts a_b in 0..k_b (commit a_b + 1 rows)
+  a_raw, b_raw [B][R][H_v] fp32   the raw projections x and z above (for raw-gating calls)
+  A_log      [H_v] fp32           the per-head decay parameter above
 """
 from __future__ import annotations
 
@@ -139,6 +141,11 @@ def make_layer(spec: LayerSpec, seed: int) -> dict:
         "ssm_state": torch.from_numpy(ssm_state),
         "g": torch.from_numpy(g.astype(np.float32)),
         "beta": torch.from_numpy(beta.astype(np.float32)),
+        # the raw gating projections g and beta come from (for callers that
+        # pass them with the raw-gating flag)
+        "a_raw": torch.from_numpy(gx.astype(np.float32)),
+        "b_raw": torch.from_numpy(bz.astype(np.float32)),
+        "A_log": torch.from_numpy(a_log.astype(np.float32)),
         "slot_ids": torch.from_numpy(slots.astype(np.int32)),
         "n_rows": torch.from_numpy(n_rows.astype(np.int32)),
         "accept_len": torch.from_numpy(acc.astype(np.int32)),

@@ -80,7 +80,9 @@ CASES = [
     ("d_v not a multiple of the block rows", dict(d_v=48), 2),
     ("H_v % H_qk", dict(H_v=24), 2),
     ("dtype", dict(in_dtype=7), 2),
-    ("flags", dict(flags=1), 1),
+    ("unknown flag", dict(flags=2), 1),
+    ("raw gating without A_log", dict(flags=1), 1),
+    ("misaligned A_log", dict(flags=1, A_log=FAKE + 2), 3),
     ("negative eps", dict(l2_eps=-1.0), 1),
     ("nan scale", dict(scale=float("nan")), 1),
     ("null x", dict(x=None), 1),

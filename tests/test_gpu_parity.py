@@ -269,3 +269,20 @@ def test_guard_bands_untouched():
     assert bool((s_buf[:G] == -9.0).all()) and bool((s_buf[-G:] == -9.0).all())
     ref = oracle.verify_commit(layer)
     assert o_error(o.double().cpu().numpy(), ref["o"], valid_rows(layer)) <= O_TOL
+
+
+RAW_CASES = [(TINY, None, "fused"), (SINGLE, None, "fused"), (SWEEP, 16, "fused"), (SWEEP, 4, "replay"),
+             (RAGGED, None, "fused"), (TINY, None, "snapshot")]
+
+
+@pytest.mark.parametrize("name,batch,mode", RAW_CASES, ids=lambda c: str(c))
+def test_raw_gating_matches_oracle(name, batch, mode):
+    """The prologue forms g = -exp(A_log) softplus(a) and beta = sigmoid(b)
+    from the raw projections (GDN_FLAG_RAW_GATING); the oracle forms them in
+    fp64 from the same fp32 inputs."""
+    ((spec, seed),) = workload_layers(name, batch=batch)
+    layer = make_layer(spec, seed)
+    ref = oracle.verify_commit(layer, commit=True, raw_gating=True)
+    dev = run_gpu(layer, mode, raw_gating=True)
+    check_against_oracle(layer, dev, ref, commit=True)
+    assert int(dev.status.item()) == 0

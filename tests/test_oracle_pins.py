@@ -18,6 +18,9 @@ Pinned:
     and special cases (beta=0 pure decay, beta=1 exact write S k = v,
     orthonormal keys keep every written value)
   * value head h reads q/k head h // (H_v / H_qk): one-hot q per q/k head.
+  * the raw gating g = -exp(A_log) softplus(a), beta = sigmoid(b): torch's own
+    softplus and sigmoid (library routines), including tails where the naive
+    forms overflow.
 """
 from __future__ import annotations
 
@@ -351,3 +354,41 @@ def test_every_mutation_is_caught(mutation):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"no pin catches mutation {mutation}"
+
+
+# ------------------------------------------------------------ raw gating
+def test_raw_gating_matches_library_softplus_and_sigmoid():
+    """oracle.gating against torch.nn.functional.softplus / torch.sigmoid in
+    fp64, with values pushed into both tails; and a raw-gating call equals a
+    call given torch's g and beta."""
+    layer = tiny_layer(seed=5)
+    a = layer["a_raw"].double().clone()
+    b = layer["b_raw"].double().clone()
+    a[0, 0, 0], a[0, 1, 0], a[1, 0, 1] = 80.0, -80.0, 1e-9
+    b[0, 0, 1], b[0, 1, 1], b[1, 0, 0] = 60.0, -60.0, 0.0
+    A_log = layer["A_log"].double()
+    g_ref = -torch.exp(A_log) * torch.nn.functional.softplus(a, threshold=1000.0)
+    beta_ref = torch.sigmoid(b)
+    g, beta = oracle.gating(a, b, A_log)
+    np.testing.assert_allclose(g, g_ref.numpy(), rtol=1e-14, atol=1e-300)
+    np.testing.assert_allclose(beta, beta_ref.numpy(), rtol=1e-14, atol=1e-300)
+    assert beta[0, 1, 1] > 0.0 and beta[0, 0, 1] <= 1.0 and np.all(g <= 0.0)
+
+    raw = oracle.verify_commit(dict(layer, a_raw=a, b_raw=b), raw_gating=True)
+    given = oracle.verify_commit(dict(layer, g=g_ref, beta=beta_ref))
+    valid = ~np.isnan(given["o"])
+    np.testing.assert_allclose(raw["o"][valid], given["o"][valid], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(raw["ssm_state"], given["ssm_state"], rtol=1e-13, atol=1e-15)
+    assert np.array_equal(raw["conv_state"], given["conv_state"])
+
+
+def test_raw_gating_tails_reduce_to_the_special_cases():
+    """a -> -inf gives g = 0 (no decay) and b -> +inf gives beta = 1, so the
+    raw call reduces to the exact-write case S k = v of the precomputed one."""
+    layer = tiny_layer(seed=6)
+    big = torch.full_like(layer["a_raw"], 1e4)
+    raw = oracle.verify_commit(dict(layer, a_raw=-big, b_raw=big), raw_gating=True)
+    given = oracle.verify_commit(dict(layer, g=torch.zeros_like(big), beta=torch.ones_like(big)))
+    valid = ~np.isnan(given["o"])
+    assert np.array_equal(raw["o"][valid], given["o"][valid])
+    assert np.array_equal(raw["ssm_state"], given["ssm_state"])
