@@ -191,6 +191,44 @@ GDN_API size_t gdn_work_bytes(const gdn_args* args);
 /* Static description of a return code (never NULL). */
 GDN_API const char* gdn_strerror(int code);
 
+/* ---- greedy acceptance of drafts on the device --------------------------
+ * The commit's accept_len decided on the device, so it feeds gdn_commit /
+ * gdn_verify_commit with no device-to-host copy [LightLLM #1330, Summary:
+ * the accept length stays on the device; FreeToken #828, Design: the
+ * target's choices decide how many drafts are kept].
+ *
+ * For every request b with 0 < n_rows[b] <= R and every verify row
+ * t < n_rows[b]:  target[b][t] = the index of the largest logits[b][t][:]
+ * (the lowest index among equal largest values; NaN entries never win).
+ * Then accept_len[b] = the largest a <= n_rows[b]-1 with drafts[b][i] ==
+ * target[b][i] for all i < a: draft i+1 is the token at verify row i+1 and
+ * is kept when the target chose it at row i.  target[b][a] is the target's
+ * token after the accepted drafts.
+ *
+ *   logits      [B][R][V]  in_dtype (bf16 or fp32), 16-byte aligned, V % 8 == 0
+ *   drafts      [B][R-1]   int32, draft i+1 of request b at [b][i] (may be NULL when R == 1)
+ *   n_rows      [B]        int32, valid rows (0 = inactive)
+ *   target      [B][R]     int32 out; rows t >= n_rows[b] are not written
+ *   accept_len  [B]        int32 out; 0 for inactive requests and for a bad n_rows
+ *   status      [1]        int32, may be NULL; GDN_STATUS_BAD_NROWS for n_rows outside [0, R]
+ *
+ * Two kernels on `stream` (a cluster of 8 CTAs per verify row, then one
+ * thread per request), chained by programmatic dependent launch; allocates
+ * nothing and does not synchronise.  Returns GDN_ERR_INVALID_ARG,
+ * GDN_ERR_UNSUPPORTED (V % 8 != 0, B or R > 65535, dtype),
+ * GDN_ERR_MISALIGNED or GDN_ERR_LAUNCH before launching anything. */
+typedef struct gdn_accept_args {
+  int32_t B, R, V;
+  int32_t in_dtype; /* GDN_DTYPE_BF16 or GDN_DTYPE_F32 */
+  const void* logits;
+  const int32_t* drafts;
+  const int32_t* n_rows;
+  int32_t* target;
+  int32_t* accept_len;
+  int32_t* status;
+} gdn_accept_args;
+GDN_API int gdn_greedy_accept(const gdn_accept_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

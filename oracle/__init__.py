@@ -58,6 +58,8 @@ def _load():
         lib.oracle_gdn_verify_commit.restype = ctypes.c_int
         lib.oracle_gdn_gating.argtypes = [ctypes.c_long, ctypes.c_int, dp, dp, dp, dp, dp]
         lib.oracle_gdn_gating.restype = None
+        lib.oracle_greedy_accept.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, dp, ip, ip, ip, ip]
+        lib.oracle_greedy_accept.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -139,3 +141,19 @@ def verify_commit(layer: dict, *, commit: bool = True, snapshot: bool = False,
     if snapshot:
         out["snap_S"], out["snap_cs"] = snap_S, snap_cs
     return out
+
+
+def greedy_accept(case: dict) -> dict:
+    """Greedy acceptance on the CPU (``oracle_greedy_accept``) for the dict
+    ``inputs.make_accept_case`` returns: target [B][R] (-1 where no row) and
+    accept_len [B]."""
+    logits = _f64(case["logits"])
+    B, R, V = logits.shape
+    drafts = _i32(case["drafts"]) if R > 1 else np.zeros((B, 1), dtype=np.int32)
+    n_rows = _i32(case["n_rows"])
+    target = np.full((B, R), -1, dtype=np.int32)
+    acc = np.zeros(B, dtype=np.int32)
+    ip = ctypes.c_int
+    status = _load().oracle_greedy_accept(B, R, V, _ptr(logits, ctypes.c_double), _ptr(drafts, ip),
+                                          _ptr(n_rows, ip), _ptr(target, ip), _ptr(acc, ip))
+    return {"target": target, "accept_len": acc, "status": int(status)}

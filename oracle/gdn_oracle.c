@@ -232,3 +232,35 @@ int oracle_gdn_verify_commit(const oracle_dims* d, const double* x, const double
   free(r);
   return status;
 }
+
+/* Greedy acceptance, written out plainly.  For each request b with
+ * 0 < n_rows[b] <= R: target[b][t] = index of the largest logits[b][t][v]
+ * over v (scanning v upward, a later entry wins only if strictly larger, so
+ * equal largest values keep the lowest index; NaN never compares larger), for
+ * t < n_rows[b]; accept_len[b] = number of leading drafts equal to the target
+ * token at the row before them: d_{i+1} = drafts[b][i] is kept while
+ * drafts[b][i] == target[b][i], at most n_rows[b]-1 drafts.  Other requests
+ * get accept_len 0 (a bad n_rows sets the returned status bit). */
+int oracle_greedy_accept(int B, int R, long V, const double* logits, const int* drafts,
+                         const int* n_rows, int* target, int* accept_len) {
+  int status = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = n_rows[b];
+    accept_len[b] = 0;
+    if (n < 0 || n > R) {
+      status |= ORACLE_BAD_NROWS;
+      continue;
+    }
+    for (int t = 0; t < n; ++t) {
+      const double* row = logits + ((long)b * R + t) * V;
+      long best = 0;
+      for (long v = 1; v < V; ++v)
+        if (row[v] > row[best] || (row[best] != row[best] && row[v] == row[v])) best = v;
+      target[(long)b * R + t] = (int)best;
+    }
+    int a = 0;
+    while (a < n - 1 && drafts[(long)b * (R - 1) + a] == target[(long)b * R + a]) ++a;
+    accept_len[b] = a;
+  }
+  return status;
+}

@@ -59,6 +59,17 @@ _lib.gdn_strerror.argtypes = [ctypes.c_int]
 _lib.gdn_strerror.restype = ctypes.c_char_p
 
 
+class GdnAcceptArgs(ctypes.Structure):
+    """Mirror of ``gdn_accept_args``."""
+
+    _fields_ = [("B", _I32), ("R", _I32), ("V", _I32), ("in_dtype", _I32), ("logits", _P), ("drafts", _P),
+                ("n_rows", _P), ("target", _P), ("accept_len", _P), ("status", _P)]
+
+
+_lib.gdn_greedy_accept.argtypes = [ctypes.POINTER(GdnAcceptArgs), _P]
+_lib.gdn_greedy_accept.restype = ctypes.c_int
+
+
 def strerror(code: int) -> str:
     return _lib.gdn_strerror(code).decode()
 
@@ -169,3 +180,21 @@ class DeviceLayer:
                          o=self.o, scratch_S=self.scratch_S, scratch_cs=self.scratch_cs,
                          work=self.work, status=self.status, H_qk=self.spec.H_qk,
                          scale=self.scale, l2_eps=self.l2_eps, A_log=self.A_log)
+
+
+def greedy_accept(logits, drafts, n_rows, target, accept_len, status=None, stream=None) -> GdnAcceptArgs:
+    """Device-side greedy acceptance (``gdn_greedy_accept``): target [B][R]
+    and accept_len [B] from logits [B][R][V] and drafts [B][R-1].  Returns
+    the argument struct (keep the tensors alive until the stream is done)."""
+    B, R, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = BF16
+    elif logits.dtype == torch.float32:
+        dt = F32
+    else:
+        raise TypeError(f"unsupported logits dtype {logits.dtype}")
+    a = GdnAcceptArgs(B=B, R=R, V=V, in_dtype=dt, logits=_ptr(logits), drafts=_ptr(drafts),
+                      n_rows=_ptr(n_rows), target=_ptr(target), accept_len=_ptr(accept_len),
+                      status=_ptr(status))
+    _check(_lib.gdn_greedy_accept(ctypes.byref(a), _stream(stream)), "gdn_greedy_accept")
+    return a

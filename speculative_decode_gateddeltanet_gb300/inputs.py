@@ -206,3 +206,44 @@ def spec_bytes(spec: LayerSpec, n_rows) -> int:
         if n > 0:
             total += s + cs + n * per_row
     return total
+
+
+def make_accept_case(B: int, R: int, V: int, seed: int, dtype: str = "bf16", inactive: int = 0,
+                     ties: bool = True) -> dict:
+    """Target logits and drafts of one greedy-acceptance call, with the
+    answers planted by construction rather than computed.
+
+    Logits are N(0, 1) clipped to [-6, 6]; each valid row gets one planted
+    token at +8, so that token is the row's largest value (with ``ties``,
+    some rows also get a second +8 at a higher index, which must lose to the
+    lower one).  Request b accepts a_b ~ U{0..k_b} drafts: drafts up to a_b
+    copy the planted tokens of the rows before them, the next one differs.
+    Returns logits, drafts [B][R-1], n_rows, and the planted target and
+    accept_len."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    logits = np.clip(rng.standard_normal((B, R, V)), -6.0, 6.0)
+    n_rows = rng.integers(1, R + 1, size=B)
+    if inactive:
+        n_rows[rng.choice(B, size=inactive, replace=False)] = 0
+    planted = rng.integers(0, V - 1, size=(B, R))
+    for b in range(B):
+        for t in range(R):
+            logits[b, t, planted[b, t]] = 8.0
+            if ties and (b + t) % 3 == 0:
+                logits[b, t, rng.integers(planted[b, t] + 1, V)] = 8.0  # a later equal maximum
+    acc = np.array([rng.integers(0, max(int(n), 1)) if n > 0 else 0 for n in n_rows])
+    drafts = rng.integers(0, V, size=(B, max(R - 1, 1)))
+    for b in range(B):
+        for i in range(R - 1):
+            if i < acc[b]:
+                drafts[b, i] = planted[b, i]
+            elif i == acc[b]:
+                drafts[b, i] = (planted[b, i] + 1) % V
+    store = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return {
+        "logits": torch.from_numpy(logits.astype(np.float32)).to(store),
+        "drafts": torch.from_numpy(drafts[:, :max(R - 1, 1)].astype(np.int32)),
+        "n_rows": torch.from_numpy(n_rows.astype(np.int32)),
+        "planted_target": planted.astype(np.int32),
+        "planted_accept": acc.astype(np.int32),
+    }

@@ -21,7 +21,7 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_work_bytes",
-                                      "gdn_strerror", "gdn_verify_commit_static"}
+                                      "gdn_strerror", "gdn_verify_commit_static", "gdn_greedy_accept"}
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):
@@ -154,3 +154,34 @@ def test_product_never_imports_the_oracle():
         text = p.read_text()
         assert "import oracle" not in text and "from oracle" not in text, p
         assert "gdn_oracle" not in text, p
+
+
+ACCEPT_CASES = [
+    ("null args", None, 1),
+    ("negative B", dict(B=-1), 1),
+    ("zero R", dict(R=0), 1),
+    ("V not a multiple of 8", dict(V=100), 2),
+    ("dtype", dict(in_dtype=5), 2),
+    ("null logits", dict(logits=None), 1),
+    ("null drafts with R > 1", dict(drafts=None), 1),
+    ("null target", dict(target=None), 1),
+    ("misaligned logits", dict(logits=FAKE + 8), 3),
+    ("misaligned accept_len", dict(accept_len=FAKE + 2), 3),
+]
+
+
+@pytest.mark.parametrize("what,over,code", ACCEPT_CASES, ids=[c[0] for c in ACCEPT_CASES])
+def test_greedy_accept_rejects_bad_arguments(cuda_lib, what, over, code):
+    if over is None:
+        assert cuda_lib._lib.gdn_greedy_accept(None, None) == code
+        return
+    a = cuda_lib.GdnAcceptArgs(B=4, R=3, V=64, in_dtype=cuda_lib.BF16, logits=FAKE, drafts=FAKE, n_rows=FAKE,
+                               target=FAKE, accept_len=FAKE, status=None)
+    for k, v in over.items():
+        setattr(a, k, v)
+    assert cuda_lib._lib.gdn_greedy_accept(ctypes.byref(a), None) == code, what
+
+
+def test_greedy_accept_empty_batch_is_a_no_op(cuda_lib):
+    a = cuda_lib.GdnAcceptArgs(B=0, R=3, V=64, in_dtype=cuda_lib.BF16)
+    assert cuda_lib._lib.gdn_greedy_accept(ctypes.byref(a), None) == cuda_lib.OK

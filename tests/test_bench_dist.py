@@ -29,6 +29,6 @@ def _rank(rank: int, world: int, port: int, out):
 
 def test_max_over_two_gloo_ranks():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 2.5, 1: 2.5}
