@@ -302,6 +302,63 @@ def run_cuda(args, rank, ws, local):
     return out
 
 
+# ------------------------------------------------------------ greedy acceptance
+def run_accept(args, rank, ws, local):
+    """Device-side greedy acceptance on the verify shape: B=16 requests of
+    4 rows over the 151936-token vocabulary in bf16, L distinct calls per
+    step (inputs larger than L2 across the step)."""
+    from speculative_decode_gateddeltanet_gb300 import build as pkg_build
+    from speculative_decode_gateddeltanet_gb300.inputs import make_accept_case
+
+    pkg_build.build()
+    from speculative_decode_gateddeltanet_gb300 import gdn
+
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    B, R, V, L = 16, 4, 151936, 12
+    calls = []
+    for i in range(L):
+        c = make_accept_case(B, R, V, seed=9000 + i)
+        calls.append({k: c[k].to(device) for k in ("logits", "drafts", "n_rows")}
+                     | {"target": torch.empty((B, R), dtype=torch.int32, device=device),
+                        "acc": torch.empty(B, dtype=torch.int32, device=device)})
+    rows = sum(int(c["n_rows"].sum()) for c in calls)
+    nbytes = sum(int(c["n_rows"].sum()) * V * 2 for c in calls)  # the valid rows' logits, read once
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for c in calls:
+            gdn.greedy_accept(c["logits"], c["drafts"], c["n_rows"], c["target"], c["acc"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1), ws) / args.steps
+    peak, peak_kind = hbm_peak()
+    gbs = nbytes / (ms_step / 1e3) / 1e9
+    return {"metric": "greedy acceptance: verify rows/s (argmax over the vocabulary + accepted prefix)",
+            "value": round(rows * ws / (ms_step / 1e3), 1), "unit": "rows/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"accept-B{B}-R{R}-V{V}", "calls_per_step": L,
+                       "l2": "inputs larger than L2: %.0f MB of logits per step" % (nbytes / 1e6)},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                         "kernel": "argmax_kernel<bf16> + accept_kernel", "traffic": None},
+            "gpu_launches": 2 * L * args.steps}
+
+
 # ------------------------------------------------------------ oracle arm
 def oracle_rows_per_second(budget_s: float, max_layers: int = 36):
     """Time the oracle on whole layers of the stack until the budget is used."""
@@ -370,6 +427,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=None, help="requests per layer (default: the workload's 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--accept", action="store_true",
+                    help="time the device-side greedy acceptance instead of the verify + commit step")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch each step's kernels on the stream instead of replaying the step captured "
                          "as a CUDA graph")
@@ -379,6 +438,8 @@ def main(argv=None):
     rank, ws, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, ws)
+    elif args.accept:
+        out = run_accept(args, rank, ws, local)
     else:
         out = run_cuda(args, rank, ws, local)
     if rank == 0 and out is not None:
