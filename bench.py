@@ -31,7 +31,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from speculative_decode_gateddeltanet_gb300.inputs import STACK, make_layer, spec_bytes, workload_layers  # noqa: E402
+from speculative_decode_gateddeltanet_gb300.inputs import (STACK, deferred_bytes, make_layer, make_step,  # noqa: E402
+                                                           spec_bytes, workload_layers)
 
 METRIC = "GDN verify+commit verified rows/sec and achieved HBM GB/s (% of peak), 1 GB300"
 UNIT = "rows/s"
@@ -179,18 +180,40 @@ def run_cuda(args, rank, ws, local):
     cargs = [d.args() for d in devs]
     stream = torch.cuda.Stream(device)
     sp = stream.cuda_stream
+    # deferred: each layer's pending rows are a previous decode step of the same shape, already on the
+    # device; the call commits their accepted prefix and verifies the current rows
+    pending, prevs = [], []
+    if args.mode == "deferred":
+        for h, d, a in zip(host, devs, cargs):
+            ps = make_step(h, h["spec"], h["seed"] + 7919)
+            t = {k: ps[k].to(device).contiguous() for k in ("x", "g", "beta", "n_rows", "accept_len")}
+            t["work"] = torch.empty(gdn.deferred_work_bytes(a, spec.R) // 4, device=device)
+            a.work = t["work"].data_ptr()
+            a.accept_len = None
+            pending.append(t)
+            prevs.append(gdn.make_prev(**{k: v for k, v in t.items() if k != "work"}))
+
+    def call(a, i):
+        if args.mode == "fused":
+            gdn.gdn_verify_commit(a, sp)
+        elif args.mode == "deferred":
+            gdn.gdn_verify_deferred(a, prevs[i], sp)
+        else:
+            m = gdn.REPLAY if args.mode == "replay" else gdn.SNAPSHOT
+            gdn.gdn_verify(a, m, sp)
+            gdn.gdn_commit(a, m, sp)
 
     def step():
-        if args.mode == "fused":
-            for a in cargs:
-                gdn.gdn_verify_commit(a, sp)
+        if args.mode in ("fused", "deferred"):
+            for i, a in enumerate(cargs):
+                call(a, i)
         else:
             m = gdn.REPLAY if args.mode == "replay" else gdn.SNAPSHOT
             for a in cargs:
                 gdn.gdn_verify(a, m, sp)
                 gdn.gdn_commit(a, m, sp)
 
-    launches_per_step = len(cargs) * (1 if args.mode == "fused" else 2)
+    launches_per_step = len(cargs) * (1 if args.mode in ("fused", "deferred") else 2)
     # --graph: the step's launches captured once into a CUDA graph and replayed
     graph = None
 
@@ -200,7 +223,11 @@ def run_cuda(args, rank, ws, local):
         else:
             step()
     rows_per_step = sum(int(h["n_rows"].clamp(min=0).sum()) for h in host)
-    bytes_per_step = sum(spec_bytes(h["spec"], h["n_rows"]) for h in host)
+    if args.mode == "deferred":
+        bytes_per_step = sum(deferred_bytes(h["spec"], h["n_rows"], t["n_rows"].cpu(), t["accept_len"].cpu())
+                             for h, t in zip(host, pending))
+    else:
+        bytes_per_step = sum(spec_bytes(h["spec"], h["n_rows"]) for h in host)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -238,22 +265,21 @@ def run_cuda(args, rank, ws, local):
 
     # ---- end to end: pinned host inputs -> device -> call -> o back to host ----
     host_in = []
-    for h in host:
+    for i, h in enumerate(host):
         host_in.append({k: h[k].pin_memory() for k in ("x", "g", "beta", "slot_ids", "n_rows", "accept_len")})
+        if args.mode == "deferred":  # the host's accept counts of the pending step replace the current ones
+            del host_in[-1]["accept_len"]
+            host_in[-1]["prev_accept_len"] = pending[i]["accept_len"].cpu().pin_memory()
     host_o = [torch.empty(d.o.shape, dtype=d.o.dtype).pin_memory() for d in devs]
     h2d = sum(t.numel() * t.element_size() for hi in host_in for t in hi.values())
     d2h = sum(t.numel() * t.element_size() for t in host_o)
 
     def e2e_step():
-        for hi, d, a, ho in zip(host_in, devs, cargs, host_o):
+        for i, (hi, d, a, ho) in enumerate(zip(host_in, devs, cargs, host_o)):
             for k, t in hi.items():
-                getattr(d, k).copy_(t, non_blocking=True)
-            if args.mode == "fused":
-                gdn.gdn_verify_commit(a, sp)
-            else:
-                m = gdn.REPLAY if args.mode == "replay" else gdn.SNAPSHOT
-                gdn.gdn_verify(a, m, sp)
-                gdn.gdn_commit(a, m, sp)
+                dst = pending[i]["accept_len"] if k == "prev_accept_len" else getattr(d, k)
+                dst.copy_(t, non_blocking=True)
+            call(a, i)
             ho.copy_(d.o, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 200))
@@ -274,7 +300,8 @@ def run_cuda(args, rank, ws, local):
     peak, peak_kind = hbm_peak()
     per_launch_bytes = bytes_per_step / len(cargs)
     launch_s = ms_step / 1e3 / launches_per_step
-    achieved = per_launch_bytes / launch_s / 1e9 if args.mode == "fused" else bytes_per_step / (ms_step / 1e3) / 1e9
+    achieved = (per_launch_bytes / launch_s / 1e9 if args.mode in ("fused", "deferred")
+                else bytes_per_step / (ms_step / 1e3) / 1e9)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
@@ -422,7 +449,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["fused", "replay", "snapshot"], default="fused")
+    ap.add_argument("--mode", choices=["fused", "replay", "snapshot", "deferred"], default="fused",
+                    help="deferred: each call commits the previous step's accepted rows and verifies the "
+                         "current ones (gdn_verify_deferred)")
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--batch", type=int, default=None, help="requests per layer (default: the workload's 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

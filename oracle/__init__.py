@@ -143,6 +143,33 @@ def verify_commit(layer: dict, *, commit: bool = True, snapshot: bool = False,
     return out
 
 
+def verify_deferred(cur: dict, prev: dict | None = None, *, requests=None, scale: float | None = None,
+                    l2_eps: float = DEFAULT_EPS, raw_gating: bool = False) -> dict:
+    """Deferred commit on the CPU, by its definition: the previous step's rows
+    0..accept_len are committed (a commit of ``prev`` that replays them from
+    the slots), then the current rows are verified from the committed slots.
+
+    ``cur`` holds the current step's rows and the weights, slot ids and slot
+    pools as they stand before the previous step's commit; ``prev`` (None =
+    nothing pending) holds the previous step's x, g, beta (a_raw, b_raw),
+    n_rows and accept_len, its own spec giving its rows per request.  Both
+    oracle calls run over ``requests`` only.  Returns o of the current rows,
+    the pools after the call and the OR of both calls' status bits."""
+    pools, status, seconds = cur, 0, 0.0
+    if prev is not None:
+        step = dict(prev)
+        for key in ("conv_w", "conv_state", "ssm_state", "slot_ids", "A_log"):
+            step[key] = cur[key]
+        r1 = verify_commit(step, commit=True, requests=requests, scale=scale, l2_eps=l2_eps,
+                           raw_gating=raw_gating)
+        pools = dict(cur, conv_state=r1["conv_state"], ssm_state=r1["ssm_state"])
+        status, seconds = r1["status"], r1["seconds"]
+    r2 = verify_commit(pools, commit=False, requests=requests, scale=scale, l2_eps=l2_eps,
+                       raw_gating=raw_gating)
+    return {"o": r2["o"], "ssm_state": r2["ssm_state"], "conv_state": r2["conv_state"],
+            "status": status | r2["status"], "seconds": seconds + r2["seconds"]}
+
+
 def greedy_accept(case: dict) -> dict:
     """Greedy acceptance on the CPU (``oracle_greedy_accept``) for the dict
     ``inputs.make_accept_case`` returns: target [B][R] (-1 where no row) and

@@ -55,7 +55,9 @@ constexpr int kMaxR = 16;         // rows per request (k <= 15)
 constexpr int kPrepThreads = 256; // channels per prologue block (>= 2 * max d_k)
 constexpr unsigned kFull = 0xffffffffu;
 
-enum Mode : int { kFused = 0, kVerify = 1, kVerifySnap = 2, kCommitReplay = 3 };
+// kDeferred: the previous step's accepted rows are replayed from the slot and
+// committed, then the current rows are verified from that state (o only).
+enum Mode : int { kFused = 0, kVerify = 1, kVerifySnap = 2, kCommitReplay = 3, kDeferred = 4 };
 
 struct Params {
   int B, R, H_qk, H_v, d_k, d_v, P, G, slices;
@@ -81,6 +83,15 @@ struct Params {
   int* status;
   const float* A_log;  // GDN_FLAG_RAW_GATING: g and beta hold the raw projections a and b
   int raw_gating;
+  // Deferred commit: request b's block of rows is the previous step's rows
+  // 0..acc_prev[b] (when n_prev[b] > 0) then its current rows; R = Rp + Rc.
+  const void* xp;      // [B][Rp][C]   the previous step's x
+  const float* gp;     // [B][Rp][H_v] its g and beta
+  const float* betap;
+  const int* n_prev;   // [B] its valid rows, 0 = nothing pending (NULL: none pending)
+  const int* acc_prev; // [B] its accepted drafts
+  int Rp;              // rows per request in the previous step's arrays
+  int Rc;              // rows per request in x, g, beta and o (= R except when deferred)
 };
 
 // Lane geometry of the rows kernel for a d_k-column state.
@@ -215,15 +226,50 @@ __device__ __forceinline__ int request_rows_of(const Params& p, int n, int slot,
   }
   return kReplay ? a + 1 : n;
 }
-// The same for request b, read from the call's arrays.
-template <bool kCommits, bool kReplay>
-__device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, int& a, bool& commit, int& report) {
+// Deferred commit: from the current n_rows n, the slot and the previous
+// step's n_prev np and accepted drafts ap.  The block of rows is ap + 1
+// previous rows (off, 0 when nothing is pending) and then the n current rows;
+// the slot is committed at row ap.  A bad ap skips the request.
+__device__ __forceinline__ int deferred_rows_of(const Params& p, int n, int slot, int np, int ap, int& off,
+                                                int& crow, int& report) {
+  report = 0;
+  crow = -1;
+  off = 0;
+  if (n == 0 && np == 0) return 0;
+  if (slot < 0 || slot >= p.P) {
+    report = GDN_STATUS_BAD_SLOT;
+    return 0;
+  }
+  if (n < 0 || n > p.Rc || np < 0 || np > p.Rp) {
+    report = GDN_STATUS_BAD_NROWS;
+    return 0;
+  }
+  if (np > 0) {
+    if (ap < 0 || ap >= np) {
+      report = GDN_STATUS_BAD_ACCEPT;
+      return 0;
+    }
+    off = ap + 1;
+    crow = ap;
+  }
+  return off + n;
+}
+// Request b's block of rows as every kernel of a call in mode MODE reads it:
+// rows to run; slot; crow = commit row (-1 none); off = leading rows that
+// are the previous step's (deferred mode; else 0); report = status bit.
+template <int MODE>
+__device__ __forceinline__ int request_block(const Params& p, int b, int& slot, int& crow, int& off, int& report) {
   slot = p.slot_ids[b];
-  a = kCommits ? p.accept_len[b] : -1;
-  int crow;
-  const int rows = request_rows_of<kCommits, kReplay>(p, p.n_rows[b], slot, a, crow, report);
-  commit = crow >= 0;
-  return rows;
+  off = 0;
+  if constexpr (MODE == kDeferred) {
+    const int np = p.n_prev ? p.n_prev[b] : 0;
+    const int ap = p.n_prev ? p.acc_prev[b] : -1;
+    return deferred_rows_of(p, p.n_rows[b], slot, np, ap, off, crow, report);
+  } else {
+    constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
+    const int a = kCommits ? p.accept_len[b] : -1;
+    return request_rows_of<kCommits, MODE == kCommitReplay>(p, p.n_rows[b], slot, a, crow, report);
+  }
 }
 
 // ------------------------------------------------------------ prologue
@@ -234,17 +280,29 @@ __device__ __forceinline__ int request_rows(const Params& p, int b, int& slot, i
 //   wsc [B][H_v][R][4]        exp(g), beta, k^.(scale q^), 0   (one run per (b, head))
 template <typename T, int MODE, int RMAX>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
-  constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
+  constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay || MODE == kDeferred;
   constexpr bool kSnap = MODE == kVerifySnap;
   pdl_wait();     // whatever ran before on the stream is complete and visible
   pdl_trigger();  // the rows kernel may start loading its state
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
 
   const int b = blockIdx.y;
-  int slot, a, report;
-  bool commit;
-  const int t_end = request_rows<kCommits, MODE == kCommitReplay>(p, b, slot, a, commit, report);
+  int slot, a, off, report;
+  const int t_end = request_block<MODE>(p, b, slot, a, off, report);
+  const bool commit = a >= 0;
   if (t_end == 0) return;  // the rows kernel records bad requests
+  // gating of row t of the request's block for value head h
+  auto load_gate = [&](int t, int h, float& gv, float& bv) {
+    if (MODE == kDeferred && t < off) {
+      const size_t i = ((size_t)b * p.Rp + t) * p.H_v + h;
+      gv = __ldg(p.gp + i);
+      bv = __ldg(p.betap + i);
+    } else {
+      const size_t i = ((size_t)b * p.Rc + (t - off)) * p.H_v + h;
+      gv = __ldg(p.g + i);
+      bv = __ldg(p.beta + i);
+    }
+  };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int DK = p.d_k;
@@ -264,20 +322,20 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
 
   // gating of the value heads that read this q/k head: loaded now, written at the end
   float g_i = 0.f, beta_i = 0.f;
-  if (qk_block && tid < p.G * t_end) {
-    const size_t gi = ((size_t)b * p.R + tid % t_end) * p.H_v + hq * p.G + tid / t_end;
-    g_i = __ldg(p.g + gi);
-    beta_i = __ldg(p.beta + gi);
-  }
+  if (qk_block && tid < p.G * t_end) load_gate(tid % t_end, hq * p.G + tid / t_end, g_i, beta_i);
   if (active) {
-    const T* xg = static_cast<const T*>(p.x) + (size_t)b * p.R * p.C + ch;
+    // channel ch of row t of the request's block
+    auto xrow = [&](int t) -> const T* {
+      if (MODE == kDeferred && t < off) return static_cast<const T*>(p.xp) + ((size_t)b * p.Rp + t) * p.C + ch;
+      return static_cast<const T*>(p.x) + ((size_t)b * p.Rc + (t - off)) * p.C + ch;
+    };
     const T* wg = static_cast<const T*>(p.conv_w) + ch * kW;
     T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
     // every load first, so they are all in flight together
     T xr[RMAX];
 #pragma unroll
     for (int t = 0; t < RMAX; ++t)
-      if (t < t_end) xr[t] = xg[(size_t)t * p.C];
+      if (t < t_end) xr[t] = *xrow(t);
     const T q0 = wg[0], q1 = wg[1], q2 = wg[2], q3 = wg[3];
     T r0 = cs[0], r1 = cs[1], r2 = cs[2];  // window, oldest first, kept as stored
     const float w0 = tof(q0), w1 = tof(q1), w2 = tof(q2), w3 = tof(q3);
@@ -429,11 +487,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   // per-row decay and write strength of the value heads that read this q/k head
   for (int i = tid; i < p.G * t_end; i += kPrepThreads) {
     const int h = hq * p.G + i / t_end, t = i % t_end;
-    if (i >= kPrepThreads) {  // more (head, row) pairs than threads: load now
-      const size_t gi = ((size_t)b * p.R + t) * p.H_v + h;
-      g_i = __ldg(p.g + gi);
-      beta_i = __ldg(p.beta + gi);
-    }
+    if (i >= kPrepThreads) load_gate(t, h, g_i, beta_i);  // more (head, row) pairs than threads: load now
     float gg = g_i, bb = beta_i;
     if (p.raw_gating) {  // g = -exp(A_log) softplus(a), beta = sigmoid(b), overflow-free forms
       gg = -expf(__ldg(p.A_log + h)) * (fmaxf(g_i, 0.f) + log1pf(expf(-fabsf(g_i))));
@@ -524,7 +578,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   constexpr int CH = 4;        // rows per chunk
   constexpr int kDup = (LPR >> ilog2(M)) - 1;  // low lane bits that repeat a row's sums
   constexpr bool kWantO = MODE != kCommitReplay;
-  constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay;
+  constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay || MODE == kDeferred;
   constexpr bool kSnap = MODE == kVerifySnap;
   constexpr uint32_t kSBytes = DVS * DK * sizeof(float);
 
@@ -539,28 +593,40 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   auto stSC = [&](int s) { return stV(s) + R * DVS; };                  // [R][4]     exp(g), beta
   auto stGH = [&](int s) { return stSC(s) + R * 4; };                   // [R][R][2]  k.k, k.q~ (padded)
   __shared__ __align__(8) uint64_t barS, barQ[2];
-  __shared__ int sMeta[2][3];  // per item parity: slot, rows to run, commit row (-1 none)
+  __shared__ int sMeta[2][4];  // per item parity: slot, rows to run, commit row (-1 none), previous rows
 
   // ---- producer side (thread 0) ----
   // An item's request data is loaded one item ahead of its use and evaluated
   // only when its copies are issued, so the producer's warp never waits on
   // those loads while the item before it computes.
   struct Req {
-    int n, slot, a;
+    int n, slot, a, np;  // np: the previous step's rows (deferred mode), a then its accepted drafts
   };
   auto load_req = [&](int it) {
     const int b = it / (p.H_v * p.slices);
     Req q;
     q.n = p.n_rows[b];
     q.slot = p.slot_ids[b];
-    q.a = kCommits ? p.accept_len[b] : -1;
+    if (MODE == kDeferred) {
+      q.np = p.n_prev ? p.n_prev[b] : 0;
+      q.a = p.n_prev ? p.acc_prev[b] : -1;
+    } else {
+      q.np = 0;
+      q.a = kCommits ? p.accept_len[b] : -1;
+    }
     return q;
   };
-  auto meta = [&](int it, const Req& q, int& slot, int& rows, int& commit_row) {
+  // item it's request data -> its row of sMeta; reports a bad request once per request
+  auto meta = [&](int it, const Req& q, int* m) {
     const int hs = it % (p.H_v * p.slices);
-    int report;
-    slot = q.slot;
-    rows = request_rows_of<kCommits, MODE == kCommitReplay>(p, q.n, q.slot, q.a, commit_row, report);
+    int report, crow, off = 0;
+    m[0] = q.slot;
+    if (MODE == kDeferred)
+      m[1] = deferred_rows_of(p, q.n, q.slot, q.np, q.a, off, crow, report);
+    else
+      m[1] = request_rows_of<kCommits, MODE == kCommitReplay>(p, q.n, q.slot, q.a, crow, report);
+    m[2] = crow;
+    m[3] = off;
     if (report && hs == 0) flag(p.status, report);
   };
   auto issue_state = [&](int it, int slot, int rows) {
@@ -596,7 +662,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   // request data.
   constexpr int kRowsProducer = Gm::NT > 32 ? 32 : 0;
   const bool producer = tid == 0 || tid == kRowsProducer;
-  Req qn{0, 0, -1};  // producer: request data of the item after the current one
+  Req qn{0, 0, -1, 0};  // producer: request data of the item after the current one
   if (tid == kRowsProducer && blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);
   if (tid == 0) {
     mbar_init(&barS, 1);
@@ -605,12 +671,8 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     if (blockIdx.x < n_items) {
       const Req q0 = load_req(blockIdx.x);
       if (blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);  // both in flight
-      int slot, rows, crow;
-      meta(blockIdx.x, q0, slot, rows, crow);
-      sMeta[0][0] = slot;
-      sMeta[0][1] = rows;
-      sMeta[0][2] = crow;
-      issue_state(blockIdx.x, slot, rows);  // before the prologue has finished
+      meta(blockIdx.x, q0, sMeta[0]);
+      issue_state(blockIdx.x, sMeta[0][0], sMeta[0][1]);  // before the prologue has finished
     }
   }
   __syncthreads();  // the barriers are initialised before anyone waits on them
@@ -638,6 +700,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       return;
     }
     const int slot = sMeta[s][0], rows = sMeta[s][1], a = sMeta[s][2];
+    const int off = MODE == kDeferred ? sMeta[s][3] : 0;  // leading rows that are the previous step's
 
     f2 S[M][NP];  // column pairs of the lane's 4-column chunks
     if (rows > 0) {
@@ -655,15 +718,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       const int it1 = it + gridDim.x;
       if (it1 < n_items) {
         fence_proxy_async();  // the reads above happen before the bulk copies overwrite the buffers
-        int nslot, nrows, ncrow;
-        meta(it1, qn, nslot, nrows, ncrow);  // loaded an item ago
+        int m[4];
+        meta(it1, qn, m);  // loaded an item ago
         if (tid == 0) {
-          sMeta[s ^ 1][0] = nslot;
-          sMeta[s ^ 1][1] = nrows;
-          sMeta[s ^ 1][2] = ncrow;
-          issue_state(it1, nslot, nrows);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sMeta[s ^ 1][j] = m[j];
+          issue_state(it1, m[0], m[1]);
         }
-        if (tid == kRowsProducer) issue_rows(s ^ 1, it1, nrows);
+        if (tid == kRowsProducer) issue_rows(s ^ 1, it1, m[1]);
         if (it1 + gridDim.x < n_items) qn = load_req(it1 + gridDim.x);  // in flight while this item computes
       }
     }
@@ -678,7 +740,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const float* sGH = stGH(s);
     float* Sg = p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK;
     float* og = nullptr;
-    if (kWantO) og = p.o + ((size_t)b * R * p.H_v + h) * p.d_v + (size_t)sl * DVS + rl;
+    if (kWantO) og = p.o + ((size_t)b * p.Rc * p.H_v + h) * p.d_v + (size_t)sl * DVS + rl;
 
     // lane's column pairs of row vector t (q at offset 0, k at offset DK)
     auto load_vec = [&](int t, int off, f2 (&vv)[NP]) {
@@ -818,7 +880,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
 #pragma unroll
             for (int x = 0; x < CH; ++x)
               if (x <= t) oo = __fmaf_rn(z[x], sGH[((c0 + x) * R + (c0 + t)) * 2 + 1], oo);
-            if (writer) og[(size_t)(c0 + t) * o_tstride] = oo;
+            if (writer && (MODE != kDeferred || c0 + t >= off)) og[(size_t)(c0 + t - off) * o_tstride] = oo;
           }
           if (kCommits && c0 + t == a) {
 #pragma unroll
@@ -852,9 +914,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) snapshot_commit_kernel(const Params p) {
   pdl_wait();  // the snapshot verify before it is complete and visible
   const int b = blockIdx.y;
-  int slot, a, report;
-  bool commit;
-  const int t_end = request_rows<true, true>(p, b, slot, a, commit, report);
+  int slot, a, off, report;  // a: the commit row
+  const int t_end = request_block<kCommitReplay>(p, b, slot, a, off, report);
   if (report && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, report);
   if (t_end == 0) return;
   const size_t slot_elems = (size_t)p.H_v * p.d_v * p.d_k;
@@ -1081,7 +1142,22 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.status = a->status;
   p.raw_gating = (a->flags & GDN_FLAG_RAW_GATING) != 0;
   p.A_log = p.raw_gating ? a->A_log : nullptr;
+  p.xp = nullptr;
+  p.gp = p.betap = nullptr;
+  p.n_prev = p.acc_prev = nullptr;
+  p.Rp = 0;
+  p.Rc = a->R;
   return GDN_OK;
+}
+
+// The deferred call's shape: the current step's arguments with R widened by
+// the previous step's rows, which is how the work buffer is sized.
+int deferred_shape(const gdn_args* cur, int prev_R, gdn_args* out) {
+  if (!cur || prev_R < 0) return GDN_ERR_INVALID_ARG;
+  if (cur->R < 1) return GDN_ERR_INVALID_ARG;
+  *out = *cur;
+  out->R = cur->R + prev_R;
+  return check_shape(out);
 }
 
 int run_rows(const gdn_args* args, unsigned need, int mode, void* stream) {
@@ -1099,6 +1175,32 @@ int run_rows(const gdn_args* args, unsigned need, int mode, void* stream) {
     default:
       return run_mode<kCommitReplay>(p, args->in_dtype, st);
   }
+}
+
+int run_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream) {
+  const int prev_R = prev ? prev->R : 0;
+  if (prev && prev->R < 1) return GDN_ERR_INVALID_ARG;
+  gdn_args a;
+  int rc = deferred_shape(cur, prev_R, &a);
+  if (rc != GDN_OK) return rc;
+  Params p;
+  rc = validate(&a, kNeedRows | kNeedO, &p);
+  if (rc != GDN_OK) return rc;
+  if (prev) {
+    if (!prev->x || !prev->g || !prev->beta || !prev->n_rows || !prev->accept_len) return GDN_ERR_INVALID_ARG;
+    if (!aligned(prev->x, 16) || !aligned(prev->g, 4) || !aligned(prev->beta, 4) || !aligned(prev->n_rows, 4) ||
+        !aligned(prev->accept_len, 4))
+      return GDN_ERR_MISALIGNED;
+    p.xp = prev->x;
+    p.gp = prev->g;
+    p.betap = prev->beta;
+    p.n_prev = prev->n_rows;
+    p.acc_prev = prev->accept_len;
+  }
+  p.Rp = prev_R;
+  p.Rc = cur->R;
+  if (p.B == 0) return GDN_OK;
+  return run_mode<kDeferred>(p, cur->in_dtype, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace gdnspec
@@ -1135,6 +1237,16 @@ GDN_API int gdn_commit(const gdn_args* args, int mode, void* stream) {
 
 GDN_API int gdn_verify_commit(const gdn_args* args, void* stream) {
   return run_rows(args, kNeedRows | kNeedO | kNeedAccept, kFused, stream);
+}
+
+GDN_API size_t gdn_deferred_work_bytes(const gdn_args* cur, int prev_R) {
+  gdn_args a;
+  if (deferred_shape(cur, prev_R, &a) != GDN_OK) return 0;
+  return sizeof(float) * work_floats(&a, nullptr, nullptr, nullptr);
+}
+
+GDN_API int gdn_verify_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream) {
+  return run_deferred(cur, prev, stream);
 }
 
 GDN_API const char* gdn_strerror(int code) {

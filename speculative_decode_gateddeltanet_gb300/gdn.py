@@ -70,6 +70,18 @@ _lib.gdn_greedy_accept.argtypes = [ctypes.POINTER(GdnAcceptArgs), _P]
 _lib.gdn_greedy_accept.restype = ctypes.c_int
 
 
+class GdnPrevRows(ctypes.Structure):
+    """Mirror of ``gdn_prev_rows``: the pending rows of a deferred commit."""
+
+    _fields_ = [("R", _I32), ("x", _P), ("g", _P), ("beta", _P), ("n_rows", _P), ("accept_len", _P)]
+
+
+_lib.gdn_verify_deferred.argtypes = [ctypes.POINTER(GdnArgs), ctypes.POINTER(GdnPrevRows), _P]
+_lib.gdn_verify_deferred.restype = ctypes.c_int
+_lib.gdn_deferred_work_bytes.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int]
+_lib.gdn_deferred_work_bytes.restype = ctypes.c_size_t
+
+
 def strerror(code: int) -> str:
     return _lib.gdn_strerror(code).decode()
 
@@ -113,6 +125,25 @@ def gdn_verify_commit_static(args: GdnArgs, stream=None) -> None:
 
 def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
+
+
+def make_prev(*, x, g, beta, n_rows, accept_len) -> GdnPrevRows:
+    """The previous step's pending rows for ``gdn_verify_deferred``: x
+    [B][R][C], g and beta [B][R][H_v], n_rows and accept_len [B]."""
+    return GdnPrevRows(R=x.shape[1], x=_ptr(x), g=_ptr(g), beta=_ptr(beta), n_rows=_ptr(n_rows),
+                       accept_len=_ptr(accept_len))
+
+
+def deferred_work_bytes(args: GdnArgs, prev_R: int) -> int:
+    """Scratch bytes of a deferred call with prev_R pending rows per request."""
+    return int(_lib.gdn_deferred_work_bytes(ctypes.byref(args), prev_R))
+
+
+def gdn_verify_deferred(args: GdnArgs, prev: GdnPrevRows | None, stream=None) -> None:
+    """Commit the previous step's accepted rows and verify the current ones in
+    one pass (``gdn_verify_deferred``); prev None = nothing pending."""
+    _check(_lib.gdn_verify_deferred(ctypes.byref(args), None if prev is None else ctypes.byref(prev),
+                                    _stream(stream)), "gdn_verify_deferred")
 
 
 def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_qk: int,

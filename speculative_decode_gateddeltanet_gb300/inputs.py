@@ -30,7 +30,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 import torch
 
-__all__ = ["LayerSpec", "make_layer", "CONFIGS", "workload_layers", "spec_bytes"]
+__all__ = ["LayerSpec", "make_layer", "make_step", "CONFIGS", "workload_layers", "spec_bytes", "deferred_bytes"]
 
 
 @dataclass(frozen=True)
@@ -152,6 +152,20 @@ def make_layer(spec: LayerSpec, seed: int) -> dict:
     }
 
 
+def make_step(prev: dict, spec: LayerSpec, seed: int) -> dict:
+    """The same layer's inputs at the next decode step: fresh rows, gating,
+    row counts and accept counts drawn as ``make_layer`` draws them (spec may
+    change k, not B, the head shapes, dtype or pool), with prev's weights,
+    A_log, slot ids and slot pools carried over."""
+    p = prev["spec"]
+    assert (spec.B, spec.H_qk, spec.H_v, spec.d_k, spec.d_v, spec.W, spec.dtype, spec.pool_slots) == \
+        (p.B, p.H_qk, p.H_v, p.d_k, p.d_v, p.W, p.dtype, p.pool_slots)
+    step = make_layer(spec, seed)
+    for key in ("conv_w", "conv_state", "ssm_state", "slot_ids", "A_log"):
+        step[key] = prev[key]
+    return step
+
+
 _QWEN = dict(H_qk=16, H_v=32, d_k=128, d_v=128)
 
 #: The workloads, by name.  The batch sweep and the 36-layer stack expand into
@@ -205,6 +219,23 @@ def spec_bytes(spec: LayerSpec, n_rows) -> int:
     for n in (int(v) for v in n_rows):
         if n > 0:
             total += s + cs + n * per_row
+    return total
+
+
+def deferred_bytes(spec: LayerSpec, n_rows, n_prev, acc_prev) -> int:
+    """Algorithmic bytes of one deferred-commit call: ``spec_bytes``'s terms
+    for every request with current or pending rows, plus the pending rows' x,
+    g and beta (acc_prev + 1 rows of each request with pending rows)."""
+    s = 2 * spec.H_v * spec.d_v * spec.d_k * 4
+    cs = 2 * spec.C * (spec.W - 1) * spec.elem_bytes
+    per_row = spec.C * spec.elem_bytes + spec.H_v * 8 + spec.H_v * spec.d_v * 4
+    pending_row = spec.C * spec.elem_bytes + spec.H_v * 8
+    total = spec.C * spec.W * spec.elem_bytes
+    for n, np_, a in zip((int(v) for v in n_rows), (int(v) for v in n_prev), (int(v) for v in acc_prev)):
+        if n > 0 or np_ > 0:
+            total += s + cs + max(n, 0) * per_row
+        if np_ > 0:
+            total += (a + 1) * pending_row
     return total
 
 

@@ -21,7 +21,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_work_bytes",
-                                      "gdn_strerror", "gdn_verify_commit_static", "gdn_greedy_accept"}
+                                      "gdn_strerror", "gdn_verify_commit_static", "gdn_greedy_accept",
+                                      "gdn_verify_deferred", "gdn_deferred_work_bytes"}
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):
@@ -35,20 +36,23 @@ def test_library_exports_every_declared_symbol(cuda_lib):
     assert not any(s.startswith("_ZN7gdnspec") for s in exported), "internal symbols leak"
 
 
-def test_struct_layout_matches_header(cuda_lib, tmp_path):
-    fields = [f[0] for f in cuda_lib.GdnArgs._fields_]
+@pytest.mark.parametrize("mirror,cname", [("GdnArgs", "gdn_args"), ("GdnAcceptArgs", "gdn_accept_args"),
+                                           ("GdnPrevRows", "gdn_prev_rows")])
+def test_struct_layout_matches_header(cuda_lib, tmp_path, mirror, cname):
+    cls = getattr(cuda_lib, mirror)
+    fields = [f[0] for f in cls._fields_]
     src = tmp_path / "layout.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdnspec.h"\nint main(void){\n'
-                   + 'printf("%zu\\n", sizeof(gdn_args));\n'
-                   + "".join(f'printf("%zu\\n", offsetof(gdn_args, {f}));\n' for f in fields)
+                   + f'printf("%zu\\n", sizeof({cname}));\n'
+                   + "".join(f'printf("%zu\\n", offsetof({cname}, {f}));\n' for f in fields)
                    + "return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-I", str(HEADER.parent), str(src), "-o", str(exe)], check=True)
     vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
                                            check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(cuda_lib.GdnArgs)
+    assert vals[0] == ctypes.sizeof(cls)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(cuda_lib.GdnArgs, f).offset == off, f
+        assert getattr(cls, f).offset == off, f
 
 
 def test_strerror_covers_codes(cuda_lib):
@@ -185,3 +189,50 @@ def test_greedy_accept_rejects_bad_arguments(cuda_lib, what, over, code):
 def test_greedy_accept_empty_batch_is_a_no_op(cuda_lib):
     a = cuda_lib.GdnAcceptArgs(B=0, R=3, V=64, in_dtype=cuda_lib.BF16)
     assert cuda_lib._lib.gdn_greedy_accept(ctypes.byref(a), None) == cuda_lib.OK
+
+
+def good_prev(gdn, **over):
+    p = gdn.GdnPrevRows(R=4, x=FAKE, g=FAKE, beta=FAKE, n_rows=FAKE, accept_len=FAKE)
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+DEFERRED_CASES = [
+    ("zero pending rows", dict(), dict(R=0), 1),
+    ("rows over 16 in all", dict(R=9), dict(R=8), 2),
+    ("null pending x", dict(), dict(x=None), 1),
+    ("null pending accept_len", dict(), dict(accept_len=None), 1),
+    ("misaligned pending x", dict(), dict(x=FAKE + 2), 3),
+    ("misaligned pending n_rows", dict(), dict(n_rows=FAKE + 1), 3),
+    ("null o", dict(o=None), dict(), 1),
+    ("null work", dict(work=None), dict(), 1),
+    ("d_k", dict(d_k=96), dict(), 2),
+]
+
+
+@pytest.mark.parametrize("what,cur,prev,code", DEFERRED_CASES, ids=[c[0] for c in DEFERRED_CASES])
+def test_deferred_rejects_bad_arguments(cuda_lib, what, cur, prev, code):
+    a, p = good_args(cuda_lib, **cur), good_prev(cuda_lib, **prev)
+    rc = cuda_lib._lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(p), None)
+    assert rc == code, (what, cuda_lib.strerror(rc))
+
+
+def test_deferred_empty_batch_and_no_pending_rows(cuda_lib):
+    lib, g = cuda_lib._lib, cuda_lib
+    a = good_args(g, B=0, accept_len=None)  # the deferred call never reads accept_len
+    assert lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(good_prev(g)), None) == g.OK
+    assert lib.gdn_verify_deferred(ctypes.byref(a), None, None) == g.OK
+    assert lib.gdn_verify_deferred(None, None, None) == g.ERR_INVALID_ARG
+    a = good_args(g, R=16)  # 16 current rows leave no room for a pending row
+    assert lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(good_prev(g, R=1)), None) == g.ERR_UNSUPPORTED
+
+
+def test_deferred_work_bytes(cuda_lib):
+    a = good_args(cuda_lib, R=3)
+    wide = good_args(cuda_lib, R=3 + 4)
+    assert cuda_lib.deferred_work_bytes(a, 4) == cuda_lib.work_bytes(wide) > cuda_lib.work_bytes(a)
+    assert cuda_lib.deferred_work_bytes(a, 0) == cuda_lib.work_bytes(a)
+    assert cuda_lib.deferred_work_bytes(a, -1) == 0
+    assert cuda_lib.deferred_work_bytes(a, 14) == 0  # 17 rows
+    assert cuda_lib._lib.gdn_deferred_work_bytes(None, 1) == 0
