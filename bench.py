@@ -177,20 +177,50 @@ def run_cuda(args, rank, ws, local):
         for d in devs:
             d.scratch_S = torch.empty((spec.B, spec.R, spec.H_v, spec.d_v, spec.d_k), device=device)
             d.scratch_cs = torch.empty((spec.B, spec.R, spec.C, spec.W - 1), dtype=d.x.dtype, device=device)
-    cargs = [d.args() for d in devs]
     stream = torch.cuda.Stream(device)
     sp = stream.cuda_stream
     # deferred: each layer's pending rows are a previous decode step of the same shape, already on the
     # device; the call commits their accepted prefix and verifies the current rows
     pending, prevs = [], []
     if args.mode == "deferred":
-        for h, d, a in zip(host, devs, cargs):
+        for h in host:
             ps = make_step(h, h["spec"], h["seed"] + 7919)
-            t = {k: ps[k].to(device).contiguous() for k in ("x", "g", "beta", "n_rows", "accept_len")}
+            pending.append({k: ps[k].to(device).contiguous() for k in ("x", "g", "beta", "n_rows", "accept_len")})
+    # A step's per-call inputs (x, g, beta, slot ids, row and accept counts) live in one device arena
+    # that one copy from a pinned host arena refills, and every layer's o in one buffer that one copy
+    # reads back: the end-to-end leg moves each step's host data in two transfers.
+    step_keys = ("x", "g", "beta", "slot_ids", "n_rows") + (("accept_len",) if args.mode != "deferred" else ())
+    parts = []
+    for i, (h, d) in enumerate(zip(host, devs)):
+        for k in step_keys:
+            parts.append((d, k, getattr(d, k)))
+        if args.mode == "deferred":
+            parts.append((pending[i], "accept_len", pending[i]["accept_len"]))
+    offs, total = [], 0
+    for _, _, t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    dev_arena = torch.zeros(total, dtype=torch.uint8, device=device)
+    host_arena = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for (owner, k, t), off in zip(parts, offs):
+        nb = t.numel() * t.element_size()
+        view = dev_arena[off:off + nb].view(t.dtype).view(t.shape)
+        view.copy_(t)
+        host_arena[off:off + nb].view(t.dtype).view(t.shape).copy_(t.cpu())
+        if isinstance(owner, dict):
+            owner[k] = view
+        else:
+            setattr(owner, k, view)
+    o_all = torch.full((len(devs),) + tuple(devs[0].o.shape), float("nan"), device=device)
+    for i, d in enumerate(devs):
+        d.o = o_all[i]
+    host_o = torch.empty(o_all.shape, dtype=o_all.dtype).pin_memory()
+    cargs = [d.args() for d in devs]
+    if args.mode == "deferred":
+        for a, t in zip(cargs, pending):
             t["work"] = torch.empty(gdn.deferred_work_bytes(a, spec.R) // 4, device=device)
             a.work = t["work"].data_ptr()
             a.accept_len = None
-            pending.append(t)
             prevs.append(gdn.make_prev(**{k: v for k, v in t.items() if k != "work"}))
 
     def call(a, i):
@@ -264,23 +294,13 @@ def run_cuda(args, rank, ws, local):
         assert int(d.status.item()) == 0, "device status bits set"
 
     # ---- end to end: pinned host inputs -> device -> call -> o back to host ----
-    host_in = []
-    for i, h in enumerate(host):
-        host_in.append({k: h[k].pin_memory() for k in ("x", "g", "beta", "slot_ids", "n_rows", "accept_len")})
-        if args.mode == "deferred":  # the host's accept counts of the pending step replace the current ones
-            del host_in[-1]["accept_len"]
-            host_in[-1]["prev_accept_len"] = pending[i]["accept_len"].cpu().pin_memory()
-    host_o = [torch.empty(d.o.shape, dtype=d.o.dtype).pin_memory() for d in devs]
-    h2d = sum(t.numel() * t.element_size() for hi in host_in for t in hi.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_o)
+    h2d = host_arena.numel()
+    d2h = host_o.numel() * host_o.element_size()
 
     def e2e_step():
-        for i, (hi, d, a, ho) in enumerate(zip(host_in, devs, cargs, host_o)):
-            for k, t in hi.items():
-                dst = pending[i]["accept_len"] if k == "prev_accept_len" else getattr(d, k)
-                dst.copy_(t, non_blocking=True)
-            call(a, i)
-            ho.copy_(d.o, non_blocking=True)
+        dev_arena.copy_(host_arena, non_blocking=True)
+        run_step()
+        host_o.copy_(o_all, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 200))
     with torch.cuda.stream(stream):

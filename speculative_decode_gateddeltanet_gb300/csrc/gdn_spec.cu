@@ -183,6 +183,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// Asks L2 to fetch [src, src + bytes) ahead of use; a hint that moves no data
+// into the CTA and orders nothing.  src and bytes are multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // Waits for phase `parity` of the barrier; gives up after a bounded number of
 // polls (each poll may itself suspend briefly) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
@@ -282,6 +287,42 @@ template <typename T, int MODE, int RMAX>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay || MODE == kDeferred;
   constexpr bool kSnap = MODE == kVerifySnap;
+  // L2 hints for this block's own inputs (its channels of the current rows of
+  // x, the slot's conv window and the taps), issued while the call waits for
+  // the work before it so the loads after the wait find them in L2.  A hint
+  // returns no data, so it may run before the wait: a slot id read early
+  // warms at worst the wrong slot, never memory outside the buffers.
+  {
+    const int b = blockIdx.y;
+    const bool qk = blockIdx.x < p.H_qk;
+    const int nrng = qk ? 2 : 1;
+    const long long vb = (long long)(blockIdx.x - p.H_qk) * kPrepThreads;
+    const long long c0 = qk ? (long long)blockIdx.x * p.d_k : 2LL * p.H_qk * p.d_k + vb;
+    const long long c1 = qk ? (long long)(p.H_qk + blockIdx.x) * p.d_k : c0;
+    const long long nch = qk ? p.d_k : min((long long)kPrepThreads, (long long)p.H_v * p.d_v - vb);
+    const int nreq = nrng * (p.Rc + 2);  // per channel range: the rows of x, the window, the taps
+    if (threadIdx.x < nreq) {
+      const int r = threadIdx.x % nrng, j = threadIdx.x / nrng;
+      const long long ch = r == 0 ? c0 : c1;
+      const char* src = nullptr;
+      size_t bytes = 0;
+      if (j < p.Rc) {
+        src = static_cast<const char*>(p.x) + (((size_t)b * p.Rc + j) * p.C + ch) * sizeof(T);
+        bytes = nch * sizeof(T);
+      } else if (j == p.Rc) {
+        const int slot = p.slot_ids[b];
+        if (slot >= 0 && slot < p.P) {
+          src = static_cast<const char*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS * sizeof(T);
+          bytes = nch * kWS * sizeof(T);
+        }
+      } else {
+        src = static_cast<const char*>(p.conv_w) + ch * kW * sizeof(T);
+        bytes = nch * kW * sizeof(T);
+      }
+      if (src != nullptr && bytes > 0 && ((reinterpret_cast<uintptr_t>(src) | bytes) & 15) == 0)
+        prefetch_l2(src, (uint32_t)bytes);
+    }
+  }
   pdl_wait();     // whatever ran before on the stream is complete and visible
   pdl_trigger();  // the rows kernel may start loading its state
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
@@ -714,6 +755,9 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         }
     }
     __syncthreads();  // the state buffer is free: request the next item
+    // On its last item the CTA lets the next call's prologue launch, so that
+    // prologue's blocks take the SMs as CTAs leave and warm their inputs.
+    if (it + gridDim.x >= n_items) pdl_trigger();
     if (producer) {
       const int it1 = it + gridDim.x;
       if (it1 < n_items) {
@@ -906,7 +950,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       if (!last) combine(c0, nc, cdec, z, true, nullptr);
     }
   }
-  pdl_trigger();  // the next call's prologue may launch once every CTA is here
+  pdl_trigger();  // CTAs that had no item
 }
 
 // Snapshot commit: slot <- scratch row accept_len[b] (state and conv window).
