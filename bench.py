@@ -31,8 +31,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from speculative_decode_gateddeltanet_gb300.inputs import (STACK, deferred_bytes, make_layer, make_step,  # noqa: E402
-                                                           spec_bytes, workload_layers)
+from speculative_decode_gateddeltanet_gb300.inputs import (CONFIGS, RAGGED, STACK, deferred_bytes,  # noqa: E402
+                                                           make_layer, make_step, spec_bytes, workload_layers)
 
 METRIC = "GDN verify+commit verified rows/sec and achieved HBM GB/s (% of peak), 1 GB300"
 UNIT = "rows/s"
@@ -148,13 +148,18 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CUDA arm
-def build_stack(layers: int, device: str, batch: int | None = None):
+def build_stack(layers: int, device: str, batch: int | None = None, workload: str = "stack"):
     from dataclasses import replace
 
     from speculative_decode_gateddeltanet_gb300 import gdn
 
     host, devs = [], []
-    for spec, seed in workload_layers(STACK, layers=layers):
+    if workload == "ragged":  # B=256 requests of 2, 4 or 9 rows, 64 value heads, 10 % inactive
+        base = CONFIGS[RAGGED]
+        specs = [(replace(base, name=f"ragged-{layers}L-B256-k1_3_8"), 4000 + i) for i in range(layers)]
+    else:
+        specs = workload_layers(STACK, layers=layers)
+    for spec, seed in specs:
         if batch is not None and batch != spec.B:
             spec = replace(spec, B=batch, name=f"qwen35-{layers}L-B{batch}-k{spec.k}")
         layer = make_layer(spec, seed)
@@ -171,7 +176,7 @@ def run_cuda(args, rank, ws, local):
 
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    host, devs = build_stack(args.layers, device, args.batch)
+    host, devs = build_stack(args.layers, device, args.batch, args.workload)
     spec = host[0]["spec"]
     if args.mode == "snapshot":
         for d in devs:
@@ -472,7 +477,11 @@ def main(argv=None):
     ap.add_argument("--mode", choices=["fused", "replay", "snapshot", "deferred"], default="fused",
                     help="deferred: each call commits the previous step's accepted rows and verifies the "
                          "current ones (gdn_verify_deferred)")
-    ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer calls per step (default 36 for the stack, 4 for the ragged batch)")
+    ap.add_argument("--workload", choices=["stack", "ragged"], default="stack",
+                    help="stack: 36 Qwen3.5-shaped layers at B=16, k=3; ragged: B=256 requests with k in "
+                         "{1,3,8} and 64 value heads (about 1 GB of state per layer)")
     ap.add_argument("--batch", type=int, default=None, help="requests per layer (default: the workload's 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -484,6 +493,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.layers is None:
+        args.layers = 4 if args.workload == "ragged" else 36
     rank, ws, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, ws)

@@ -53,6 +53,11 @@ constexpr int kW = 4;             // conv width the kernels are built for
 constexpr int kWS = kW - 1;       // conv-state columns
 constexpr int kMaxR = 16;         // rows per request (k <= 15)
 constexpr int kPrepThreads = 256; // channels per prologue block (>= 2 * max d_k)
+// value channels per prologue thread: four (one chunk load per row) when a
+// request has at most 4 rows; with more rows the extra registers would cost
+// more resident blocks than the wider loads gain
+template <int RMAX>
+__host__ __device__ constexpr int vec_v() { return RMAX <= 4 ? 4 : 1; }
 constexpr unsigned kFull = 0xffffffffu;
 
 // kDeferred: the previous step's accepted rows are replayed from the slot and
@@ -145,6 +150,19 @@ __device__ __forceinline__ float tof<__nv_bfloat16>(__nv_bfloat16 v) { return __
 
 // SiLU with the fast exponential and division (a few ulp; the conv output feeds
 // a normalisation and a dot product, far below the path's tolerance).
+// N consecutive elements of T as one aligned load or store
+template <typename T, int N>
+struct ChunkOf {
+  using type = T;
+};
+template <>
+struct ChunkOf<float, 4> {
+  using type = float4;
+};
+template <>
+struct ChunkOf<__nv_bfloat16, 4> {
+  using type = uint2;
+};
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, __fadd_rn(1.0f, __expf(-z))); }
 
 __device__ __forceinline__ void flag(int* status, int bit) {
@@ -278,8 +296,9 @@ __device__ __forceinline__ int request_block(const Params& p, int b, int& slot, 
 }
 
 // ------------------------------------------------------------ prologue
-// grid (H_qk + ceil(H_v d_v / 256), B): block x < H_qk holds the 2 d_k q and k
-// channels of q/k head x, the other blocks 256 v channels each.  Work layout:
+// grid (H_qk + ceil(H_v d_v / (256 VV)), B): block x < H_qk holds the 2 d_k q
+// and k channels of q/k head x (one per thread), the other blocks 256 VV v
+// channels each (VV consecutive channels per thread).  Work layout:
 //   wqk [B][H_qk][R][2 d_k]   scale*q^ | k^       (one contiguous run per (b, q/k head))
 //   wv  [B][H_v d_v/DVS][R][DVS]  v               (one run per (b, head, row slice))
 //   wsc [B][H_v][R][4]        exp(g), beta, k^.(scale q^), 0   (one run per (b, head))
@@ -296,10 +315,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     const int b = blockIdx.y;
     const bool qk = blockIdx.x < p.H_qk;
     const int nrng = qk ? 2 : 1;
-    const long long vb = (long long)(blockIdx.x - p.H_qk) * kPrepThreads;
+    const long long vb = (long long)(blockIdx.x - p.H_qk) * kPrepThreads * vec_v<RMAX>();
     const long long c0 = qk ? (long long)blockIdx.x * p.d_k : 2LL * p.H_qk * p.d_k + vb;
     const long long c1 = qk ? (long long)(p.H_qk + blockIdx.x) * p.d_k : c0;
-    const long long nch = qk ? p.d_k : min((long long)kPrepThreads, (long long)p.H_v * p.d_v - vb);
+    const long long nch = qk ? p.d_k : min((long long)kPrepThreads * vec_v<RMAX>(), (long long)p.H_v * p.d_v - vb);
     const int nreq = nrng * (p.Rc + 2);  // per channel range: the rows of x, the window, the taps
     if (threadIdx.x < nreq) {
       const int r = threadIdx.x % nrng, j = threadIdx.x / nrng;
@@ -349,21 +368,90 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   const int DK = p.d_k;
   const bool qk_block = blockIdx.x < p.H_qk;
   const int hq = blockIdx.x;
-  long long ch;
-  bool active;
-  int vi = 0;
-  if (qk_block) {
-    active = tid < 2 * DK;
-    ch = tid < DK ? (long long)hq * DK + tid : (long long)p.H_qk * DK + (long long)hq * DK + (tid - DK);
-  } else {
-    vi = (blockIdx.x - p.H_qk) * kPrepThreads + tid;
-    active = vi < p.H_v * p.d_v;
-    ch = 2LL * p.H_qk * DK + vi;
+
+  if (!qk_block) {
+    // value channels: VV consecutive channels per thread, loaded and stored
+    // as one chunk per row; conv + SiLU only (no norm), written as v rows
+    constexpr int VV = vec_v<RMAX>();
+    using Chunk = typename ChunkOf<T, VV>::type;
+    const int v0 = ((blockIdx.x - p.H_qk) * kPrepThreads + tid) * VV;
+    if (v0 >= p.H_v * p.d_v) return;
+    const long long cv = 2LL * p.H_qk * DK + v0;
+    auto xrow = [&](int t) -> const Chunk* {
+      const T* base = MODE == kDeferred && t < off
+                          ? static_cast<const T*>(p.xp) + ((size_t)b * p.Rp + t) * p.C
+                          : static_cast<const T*>(p.x) + ((size_t)b * p.Rc + (t - off)) * p.C;
+      return reinterpret_cast<const Chunk*>(base + cv);
+    };
+    const Chunk* wg = reinterpret_cast<const Chunk*>(static_cast<const T*>(p.conv_w) + cv * kW);
+    Chunk* cs = reinterpret_cast<Chunk*>(static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + cv) * kWS);
+    Chunk xr[RMAX];
+#pragma unroll
+    for (int t = 0; t < RMAX; ++t)
+      if (t < t_end) xr[t] = *xrow(t);
+    Chunk wc[kW], rc[kWS];
+#pragma unroll
+    for (int i = 0; i < kW; ++i) wc[i] = wg[i];
+#pragma unroll
+    for (int i = 0; i < kWS; ++i) rc[i] = cs[i];
+    const T* we = reinterpret_cast<const T*>(wc);  // [channel][tap]
+    T* re = reinterpret_cast<T*>(rc);               // [channel][window column], oldest first
+    float w[VV][kW];
+#pragma unroll
+    for (int j = 0; j < VV; ++j)
+#pragma unroll
+      for (int i = 0; i < kW; ++i) w[j][i] = tof(we[j * kW + i]);
+    Chunk cc[kWS];  // window after row a
+#pragma unroll
+    for (int i = 0; i < kWS; ++i) cc[i] = rc[i];
+    float* vdst = p.wv + (((size_t)b * p.H_v * p.slices + v0 / p.dvs) * p.R) * p.dvs + (v0 % p.dvs);
+#pragma unroll
+    for (int t = 0; t < RMAX; ++t) {
+      if (t < t_end) {
+        const T* xe = reinterpret_cast<const T*>(&xr[t]);
+        float y[VV];
+#pragma unroll
+        for (int j = 0; j < VV; ++j) {
+          T* r = re + j * kWS;
+          float z = __fmul_rn(w[j][0], tof(r[0]));
+          z = __fmaf_rn(w[j][1], tof(r[1]), z);
+          z = __fmaf_rn(w[j][2], tof(r[2]), z);
+          z = __fmaf_rn(w[j][3], tof(xe[j]), z);
+          y[j] = silu(z);
+          r[0] = r[1];
+          r[1] = r[2];
+          r[2] = xe[j];
+        }
+        if constexpr (VV == 4)
+          *reinterpret_cast<float4*>(vdst + (size_t)t * p.dvs) = make_float4(y[0], y[1], y[2], y[3]);
+        else
+          vdst[(size_t)t * p.dvs] = y[0];
+        if (kSnap) {
+          Chunk* sc = reinterpret_cast<Chunk*>(static_cast<T*>(p.snapCs) + (((size_t)b * p.R + t) * p.C + cv) * kWS);
+#pragma unroll
+          for (int i = 0; i < kWS; ++i) sc[i] = rc[i];
+        }
+        if (kCommits && t == a) {
+#pragma unroll
+          for (int i = 0; i < kWS; ++i) cc[i] = rc[i];
+        }
+      }
+    }
+    if (kCommits && commit) {  // this thread was these channels' only reader in the call
+#pragma unroll
+      for (int i = 0; i < kWS; ++i) cs[i] = cc[i];
+    }
+    return;
   }
+
+  // q/k blocks: one channel per thread, q channels of head hq then its k channels
+  const bool active = tid < 2 * DK;
+  const long long ch =
+      tid < DK ? (long long)hq * DK + tid : (long long)p.H_qk * DK + (long long)hq * DK + (tid - DK);
 
   // gating of the value heads that read this q/k head: loaded now, written at the end
   float g_i = 0.f, beta_i = 0.f;
-  if (qk_block && tid < p.G * t_end) load_gate(tid % t_end, hq * p.G + tid / t_end, g_i, beta_i);
+  if (tid < p.G * t_end) load_gate(tid % t_end, hq * p.G + tid / t_end, g_i, beta_i);
   if (active) {
     // channel ch of row t of the request's block
     auto xrow = [&](int t) -> const T* {
@@ -381,9 +469,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     T r0 = cs[0], r1 = cs[1], r2 = cs[2];  // window, oldest first, kept as stored
     const float w0 = tof(q0), w1 = tof(q1), w2 = tof(q2), w3 = tof(q3);
     T c0 = r0, c1 = r1, c2 = r2;  // window after row a
-    float* vdst = nullptr;
-    if (!qk_block)
-      vdst = p.wv + (((size_t)b * p.H_v * p.slices + vi / p.dvs) * p.R) * p.dvs + (vi % p.dvs);
 #pragma unroll
     for (int t = 0; t < RMAX; ++t) {
       if (t < t_end) {
@@ -392,11 +477,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
         z = __fmaf_rn(w1, tof(r1), z);
         z = __fmaf_rn(w2, tof(r2), z);
         z = __fmaf_rn(w3, tof(r3), z);
-        const float y = silu(z);
-        if (qk_block)
-          sy[t][tid] = y;
-        else
-          vdst[(size_t)t * p.dvs] = y;
+        sy[t][tid] = silu(z);
         r0 = r1;
         r1 = r2;
         r2 = r3;
@@ -419,7 +500,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
       cs[2] = c2;
     }
   }
-  if (!qk_block) return;
   __syncthreads();
   // Raw dot products of the rows' conv outputs, packed in n-row order: entries
   // e < n are q_t.q_t, then pairs (s, t) at n + 2 (s n + t) + {0: k_s.k_t,
@@ -1053,7 +1133,9 @@ int dispatch_rows(const Params& p, cudaStream_t st) {
 
 template <typename T, int MODE, int RMAX>
 int launch_prep_r(const Params& p, cudaStream_t st) {
-  const dim3 grid(p.H_qk + (p.H_v * p.d_v + kPrepThreads - 1) / kPrepThreads, p.B), block(kPrepThreads);
+  constexpr int VV = vec_v<RMAX>();
+  const int v_blocks = (p.H_v * p.d_v + kPrepThreads * VV - 1) / (kPrepThreads * VV);
+  const dim3 grid(p.H_qk + v_blocks, p.B), block(kPrepThreads);
   static int set_on = -1;  // device on which this instantiation's carveout was last set
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
