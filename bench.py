@@ -222,11 +222,20 @@ def run_cuda(args, rank, ws, local):
     host_o = torch.empty(o_all.shape, dtype=o_all.dtype).pin_memory()
     cargs = [d.args() for d in devs]
     if args.mode == "deferred":
-        for a, t in zip(cargs, pending):
-            t["work"] = torch.empty(gdn.deferred_work_bytes(a, spec.R) // 4, device=device)
-            a.work = t["work"].data_ptr()
+        # one untimed deferred call per layer with nothing pending writes the pending step's carry;
+        # every timed call then commits that step's accepted rows from it and writes its own carry
+        for d, a, t in zip(devs, cargs, pending):
+            t["carry_in"] = torch.empty(gdn.carry_bytes(a) // 4, device=device)
+            t["carry_out"] = torch.empty_like(t["carry_in"])
+            first = gdn.make_args(x=t["x"], g=t["g"], beta=t["beta"], conv_w=d.conv_w, conv_state=d.conv_state,
+                                  ssm_state=d.ssm_state, slot_ids=d.slot_ids, n_rows=t["n_rows"], o=d.o,
+                                  work=d.work, status=d.status, H_qk=spec.H_qk, carry=t["carry_in"])
+            gdn.gdn_verify_deferred(first, None, sp)
+            a.carry = t["carry_out"].data_ptr()
             a.accept_len = None
-            prevs.append(gdn.make_prev(**{k: v for k, v in t.items() if k != "work"}))
+            prevs.append(gdn.make_prev(x=t["x"], n_rows=t["n_rows"], accept_len=t["accept_len"],
+                                       carry=t["carry_in"]))
+        torch.cuda.synchronize()
 
     def call(a, i):
         if args.mode == "fused":
@@ -475,8 +484,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--mode", choices=["fused", "replay", "snapshot", "deferred"], default="fused",
-                    help="deferred: each call commits the previous step's accepted rows and verifies the "
-                         "current ones (gdn_verify_deferred)")
+                    help="deferred: each call commits the previous step's accepted rows from that step's "
+                         "carry and verifies the current ones (gdn_verify_deferred)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layer calls per step (default 36 for the stack, 4 for the ragged batch)")
     ap.add_argument("--workload", choices=["stack", "ragged"], default="stack",

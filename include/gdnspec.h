@@ -138,6 +138,8 @@ typedef struct gdn_args {
   void* work;                /* verify, replay commit and fused calls          */
   int32_t* status;           /* may be NULL                                    */
   const float* A_log;        /* GDN_FLAG_RAW_GATING only (4-byte aligned)      */
+  void* carry;               /* gdn_verify_deferred only: this call's carry out
+                                (gdn_carry_bytes bytes, 16-byte aligned)       */
 } gdn_args;
 
 /* Verify: for every active request, run rows 0..n_rows-1 from its slot's
@@ -194,44 +196,49 @@ GDN_API const char* gdn_strerror(int code);
 /* ---- deferred commit ------------------------------------------------------
  * Step s's verify also commits step s-1, so each step makes one pass over the
  * state: the slot keeps the state from before step s-1 until step s's call,
- * which first runs the previous step's accepted rows 0..accept_len (their
- * accept count carried over from step s-1 [LightLLM #1330, Summary: the
- * accept-count carry; lmdeploy #5006, Verification path: verify-and-commit
- * mode and draft carry]), commits the slot at the last of them, and then runs
- * the current rows from there, writing their o.  The current rows stay
- * pending for the next call.  The pages carry the count to the next step
- * without printing where the state commit happens; folding it into the next
- * verify is this library's form of it.
+ * which first commits the previous call's rows 0..accept_len (their accept
+ * count carried over from step s-1 [LightLLM #1330, Summary: the accept-count
+ * carry; lmdeploy #5006, Verification path: verify-and-commit mode and draft
+ * carry]) and then runs the current rows from there, writing their o.  The
+ * pages carry the count to the next step without printing where the state
+ * commit happens; folding it into the next verify is this library's form of it.
  *
- * prev describes the pending rows, all arrays laid out like gdn_args's with
- * prev->R rows per request:
- *   x           [B][R][C]     in_dtype  the previous step's pre-conv rows (16-byte aligned)
- *   g, beta     [B][R][H_v]   fp32      its gating (raw a and b under GDN_FLAG_RAW_GATING)
+ * The commit needs no replay: each deferred call leaves, in its carry buffer
+ * (cur->carry, gdn_carry_bytes(cur) bytes, contents private to the library),
+ * what committing any prefix of its rows takes: per row, the rank-one update
+ * of every state row (u_t in S_t = exp(g_t) S_{t-1} + u_t k_t^T), k_t and the
+ * decay.  The next call reads that carry as prev->carry and forms
+ * S_a = (prod alpha) S + sum_{t<=a} (u_t prod_{j>t} alpha_j) k_t^T.
+ *
+ * prev describes the pending rows, with prev->R rows per request:
+ *   x           [B][R][C]     in_dtype  the previous call's pre-conv rows (16-byte
+ *                                       aligned); rows 0..accept_len advance the conv window
  *   n_rows      [B]           int32     its valid rows; 0 = nothing pending for request b
  *   accept_len  [B]           int32     its accepted drafts, 0..n_rows-1 when n_rows > 0
- * prev may be NULL (nothing pending for any request: the first step).  For
- * request b the rows run are accept_len + 1 pending rows (none when its
- * prev n_rows is 0) and then cur->n_rows[b] current rows, at most
- * cur->R + prev->R <= 16 in all.  The result equals gdn_commit (replay) of the
- * previous step followed by gdn_verify of the current one.  A pending
- * accept_len outside [0, n_rows-1] or an n_rows outside [0, R] skips the
- * request and sets the matching status bit.  cur->accept_len is not read.
- * Needs cur's verify inputs (x, g, beta, conv_w, conv_state, ssm_state,
- * slot_ids, n_rows, o) and a work buffer of gdn_deferred_work_bytes(cur,
- * prev ? prev->R : 0) bytes. */
+ *   carry                               the previous deferred call's cur->carry, unchanged
+ * prev may be NULL (nothing pending for any request: the first step).  The
+ * result equals gdn_commit (replay) of the previous step followed by
+ * gdn_verify of the current one.  prev->R <= 16, like every R.  Only the
+ * last three of the pending rows 0..accept_len are read from prev->x (the
+ * conv window they leave).  A pending accept_len outside [0, n_rows-1]
+ * or an n_rows outside [0, R] skips the request and sets the matching status
+ * bit.  Carry rows of a request that a call skipped (a status bit) are
+ * undefined; cur->accept_len is not read.  Needs cur's verify inputs (x, g,
+ * beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, o), a work buffer of
+ * gdn_work_bytes(cur) bytes and cur->carry. */
 typedef struct gdn_prev_rows {
-  int32_t R;                 /* rows per request in the arrays below, >= 1 */
+  int32_t R;                 /* rows per request of the previous call, >= 1 */
   const void* x;
-  const float* g;
-  const float* beta;
   const int32_t* n_rows;
   const int32_t* accept_len;
+  const void* carry;
 } gdn_prev_rows;
 GDN_API int gdn_verify_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream);
 
-/* Work bytes of a deferred call: gdn_work_bytes with R = cur->R + prev_R;
- * 0 if the shapes are invalid, unsupported or prev_R < 0. */
-GDN_API size_t gdn_deferred_work_bytes(const gdn_args* cur, int prev_R);
+/* Bytes of carry a deferred call with these shapes writes:
+ * 4 * (B * R * (H_v * d_v + H_qk * d_k) + B * H_v * R4), R4 = R rounded up to
+ * a multiple of 4.  0 if the shapes are invalid or unsupported. */
+GDN_API size_t gdn_carry_bytes(const gdn_args* args);
 
 /* ---- greedy acceptance of drafts on the device --------------------------
  * The commit's accept_len decided on the device, so it feeds gdn_commit /

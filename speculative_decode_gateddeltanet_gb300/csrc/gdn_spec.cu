@@ -60,8 +60,9 @@ template <int RMAX>
 __host__ __device__ constexpr int vec_v() { return RMAX <= 4 ? 4 : 1; }
 constexpr unsigned kFull = 0xffffffffu;
 
-// kDeferred: the previous step's accepted rows are replayed from the slot and
-// committed, then the current rows are verified from that state (o only).
+// kDeferred: the previous call's accepted rows are committed from its carry
+// (per row: the state rows' update vectors, k^ and the decay), then the
+// current rows are verified from that state (o, and their own carry).
 enum Mode : int { kFused = 0, kVerify = 1, kVerifySnap = 2, kCommitReplay = 3, kDeferred = 4 };
 
 struct Params {
@@ -88,16 +89,23 @@ struct Params {
   int* status;
   const float* A_log;  // GDN_FLAG_RAW_GATING: g and beta hold the raw projections a and b
   int raw_gating;
-  // Deferred commit: request b's block of rows is the previous step's rows
-  // 0..acc_prev[b] (when n_prev[b] > 0) then its current rows; R = Rp + Rc.
-  const void* xp;      // [B][Rp][C]   the previous step's x
-  const float* gp;     // [B][Rp][H_v] its g and beta
-  const float* betap;
-  const int* n_prev;   // [B] its valid rows, 0 = nothing pending (NULL: none pending)
-  const int* acc_prev; // [B] its accepted drafts
-  int Rp;              // rows per request in the previous step's arrays
-  int Rc;              // rows per request in x, g, beta and o (= R except when deferred)
+  // Deferred commit.  Request b's block of conv rows is the previous call's
+  // rows 0..acc_prev[b] (when n_prev[b] > 0; they only advance the window)
+  // then its current rows.  The state rows run the current rows only, after
+  // committing the previous rows from the previous call's carry.
+  const void* xp;       // [B][Rp][C] the previous call's x
+  const int* n_prev;    // [B] its valid rows, 0 = nothing pending (NULL: none pending)
+  const int* acc_prev;  // [B] its accepted drafts
+  const float* pcu;     // carry in:  [B][H_v d_v / dvs][Rp][dvs]  u, the state rows' update vectors
+  const float* pck;     //            [B][H_qk][Rp][d_k]           k^
+  const float* pca;     //            [B][H_v][Rp4]                exp(g)
+  float* cu;            // carry out: the same for this call's rows (R, R4)
+  float* ck;
+  float* ca;
+  int Rp;               // rows per request of the previous call (0: none)
 };
+
+__host__ __device__ constexpr int round4(int r) { return (r + 3) & ~3; }
 
 // Lane geometry of the rows kernel for a d_k-column state.
 template <int DK>
@@ -250,9 +258,9 @@ __device__ __forceinline__ int request_rows_of(const Params& p, int n, int slot,
   return kReplay ? a + 1 : n;
 }
 // Deferred commit: from the current n_rows n, the slot and the previous
-// step's n_prev np and accepted drafts ap.  The block of rows is ap + 1
+// call's n_prev np and accepted drafts ap.  The block of conv rows is ap + 1
 // previous rows (off, 0 when nothing is pending) and then the n current rows;
-// the slot is committed at row ap.  A bad ap skips the request.
+// the slot is committed after previous row ap.  A bad ap skips the request.
 __device__ __forceinline__ int deferred_rows_of(const Params& p, int n, int slot, int np, int ap, int& off,
                                                 int& crow, int& report) {
   report = 0;
@@ -263,7 +271,7 @@ __device__ __forceinline__ int deferred_rows_of(const Params& p, int n, int slot
     report = GDN_STATUS_BAD_SLOT;
     return 0;
   }
-  if (n < 0 || n > p.Rc || np < 0 || np > p.Rp) {
+  if (n < 0 || n > p.R || np < 0 || np > p.Rp) {
     report = GDN_STATUS_BAD_NROWS;
     return 0;
   }
@@ -319,16 +327,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     const long long c0 = qk ? (long long)blockIdx.x * p.d_k : 2LL * p.H_qk * p.d_k + vb;
     const long long c1 = qk ? (long long)(p.H_qk + blockIdx.x) * p.d_k : c0;
     const long long nch = qk ? p.d_k : min((long long)kPrepThreads * vec_v<RMAX>(), (long long)p.H_v * p.d_v - vb);
-    const int nreq = nrng * (p.Rc + 2);  // per channel range: the rows of x, the window, the taps
+    const int nreq = nrng * (p.R + 2);  // per channel range: the rows of x, the window, the taps
     if (threadIdx.x < nreq) {
       const int r = threadIdx.x % nrng, j = threadIdx.x / nrng;
       const long long ch = r == 0 ? c0 : c1;
       const char* src = nullptr;
       size_t bytes = 0;
-      if (j < p.Rc) {
-        src = static_cast<const char*>(p.x) + (((size_t)b * p.Rc + j) * p.C + ch) * sizeof(T);
+      if (j < p.R) {
+        src = static_cast<const char*>(p.x) + (((size_t)b * p.R + j) * p.C + ch) * sizeof(T);
         bytes = nch * sizeof(T);
-      } else if (j == p.Rc) {
+      } else if (j == p.R) {
         const int slot = p.slot_ids[b];
         if (slot >= 0 && slot < p.P) {
           src = static_cast<const char*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS * sizeof(T);
@@ -351,17 +359,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   const int t_end = request_block<MODE>(p, b, slot, a, off, report);
   const bool commit = a >= 0;
   if (t_end == 0) return;  // the rows kernel records bad requests
-  // gating of row t of the request's block for value head h
-  auto load_gate = [&](int t, int h, float& gv, float& bv) {
-    if (MODE == kDeferred && t < off) {
-      const size_t i = ((size_t)b * p.Rp + t) * p.H_v + h;
-      gv = __ldg(p.gp + i);
-      bv = __ldg(p.betap + i);
-    } else {
-      const size_t i = ((size_t)b * p.Rc + (t - off)) * p.H_v + h;
-      gv = __ldg(p.g + i);
-      bv = __ldg(p.beta + i);
-    }
+  // Block rows t < off are the previous call's (deferred mode): they only
+  // advance the conv window.  The current rows t >= off are outputs r = t - off.
+  const int n = t_end - off;
+  // gating of current row r for value head h
+  auto load_gate = [&](int r, int h, float& gv, float& bv) {
+    const size_t i = ((size_t)b * p.R + r) * p.H_v + h;
+    gv = __ldg(p.g + i);
+    bv = __ldg(p.beta + i);
   };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -377,18 +382,22 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     const int v0 = ((blockIdx.x - p.H_qk) * kPrepThreads + tid) * VV;
     if (v0 >= p.H_v * p.d_v) return;
     const long long cv = 2LL * p.H_qk * DK + v0;
-    auto xrow = [&](int t) -> const Chunk* {
-      const T* base = MODE == kDeferred && t < off
-                          ? static_cast<const T*>(p.xp) + ((size_t)b * p.Rp + t) * p.C
-                          : static_cast<const T*>(p.x) + ((size_t)b * p.Rc + (t - off)) * p.C;
-      return reinterpret_cast<const Chunk*>(base + cv);
-    };
     const Chunk* wg = reinterpret_cast<const Chunk*>(static_cast<const T*>(p.conv_w) + cv * kW);
     Chunk* cs = reinterpret_cast<Chunk*>(static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + cv) * kWS);
-    Chunk xr[RMAX];
+    // every load first, so they are all in flight together: the current rows
+    // and (deferred) the last kWS of the previous call's rows 0..off-1
+    Chunk xr[RMAX], xq[kWS];
 #pragma unroll
     for (int t = 0; t < RMAX; ++t)
-      if (t < t_end) xr[t] = *xrow(t);
+      if (t < n) xr[t] = *reinterpret_cast<const Chunk*>(static_cast<const T*>(p.x) + ((size_t)b * p.R + t) * p.C + cv);
+    if (MODE == kDeferred) {
+#pragma unroll
+      for (int i = 0; i < kWS; ++i) {
+        const int t = off - kWS + i;
+        if (t >= 0)
+          xq[i] = *reinterpret_cast<const Chunk*>(static_cast<const T*>(p.xp) + ((size_t)b * p.Rp + t) * p.C + cv);
+      }
+    }
     Chunk wc[kW], rc[kWS];
 #pragma unroll
     for (int i = 0; i < kW; ++i) wc[i] = wg[i];
@@ -401,13 +410,28 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     for (int j = 0; j < VV; ++j)
 #pragma unroll
       for (int i = 0; i < kW; ++i) w[j][i] = tof(we[j * kW + i]);
-    Chunk cc[kWS];  // window after row a
+    if (MODE == kDeferred) {  // the window after the previous call's rows: the one the slot commits
+#pragma unroll
+      for (int i = 0; i < kWS; ++i) {
+        if (off - kWS + i >= 0) {
+          const T* xe = reinterpret_cast<const T*>(&xq[i]);
+#pragma unroll
+          for (int j = 0; j < VV; ++j) {
+            T* r = re + j * kWS;
+            r[0] = r[1];
+            r[1] = r[2];
+            r[2] = xe[j];
+          }
+        }
+      }
+    }
+    Chunk cc[kWS];  // window after row a (deferred: after the previous rows)
 #pragma unroll
     for (int i = 0; i < kWS; ++i) cc[i] = rc[i];
     float* vdst = p.wv + (((size_t)b * p.H_v * p.slices + v0 / p.dvs) * p.R) * p.dvs + (v0 % p.dvs);
 #pragma unroll
     for (int t = 0; t < RMAX; ++t) {
-      if (t < t_end) {
+      if (t < n) {
         const T* xe = reinterpret_cast<const T*>(&xr[t]);
         float y[VV];
 #pragma unroll
@@ -422,16 +446,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
           r[1] = r[2];
           r[2] = xe[j];
         }
+        float* vd = vdst + (size_t)t * p.dvs;
         if constexpr (VV == 4)
-          *reinterpret_cast<float4*>(vdst + (size_t)t * p.dvs) = make_float4(y[0], y[1], y[2], y[3]);
+          *reinterpret_cast<float4*>(vd) = make_float4(y[0], y[1], y[2], y[3]);
         else
-          vdst[(size_t)t * p.dvs] = y[0];
+          vd[0] = y[0];
         if (kSnap) {
           Chunk* sc = reinterpret_cast<Chunk*>(static_cast<T*>(p.snapCs) + (((size_t)b * p.R + t) * p.C + cv) * kWS);
 #pragma unroll
           for (int i = 0; i < kWS; ++i) sc[i] = rc[i];
         }
-        if (kCommits && t == a) {
+        if (kCommits && MODE != kDeferred && t == a) {
 #pragma unroll
           for (int i = 0; i < kWS; ++i) cc[i] = rc[i];
         }
@@ -451,27 +476,41 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
 
   // gating of the value heads that read this q/k head: loaded now, written at the end
   float g_i = 0.f, beta_i = 0.f;
-  if (tid < p.G * t_end) load_gate(tid % t_end, hq * p.G + tid / t_end, g_i, beta_i);
+  if (tid < p.G * n) load_gate(tid % n, hq * p.G + tid / n, g_i, beta_i);
   if (active) {
     // channel ch of row t of the request's block
-    auto xrow = [&](int t) -> const T* {
-      if (MODE == kDeferred && t < off) return static_cast<const T*>(p.xp) + ((size_t)b * p.Rp + t) * p.C + ch;
-      return static_cast<const T*>(p.x) + ((size_t)b * p.Rc + (t - off)) * p.C + ch;
-    };
     const T* wg = static_cast<const T*>(p.conv_w) + ch * kW;
     T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
-    // every load first, so they are all in flight together
-    T xr[RMAX];
+    // every load first, so they are all in flight together: the current rows
+    // and (deferred) the last kWS of the previous call's rows 0..off-1
+    T xr[RMAX], xq[kWS];
 #pragma unroll
     for (int t = 0; t < RMAX; ++t)
-      if (t < t_end) xr[t] = *xrow(t);
+      if (t < n) xr[t] = static_cast<const T*>(p.x)[((size_t)b * p.R + t) * p.C + ch];
+    if (MODE == kDeferred) {
+#pragma unroll
+      for (int i = 0; i < kWS; ++i) {
+        const int t = off - kWS + i;
+        if (t >= 0) xq[i] = static_cast<const T*>(p.xp)[((size_t)b * p.Rp + t) * p.C + ch];
+      }
+    }
     const T q0 = wg[0], q1 = wg[1], q2 = wg[2], q3 = wg[3];
     T r0 = cs[0], r1 = cs[1], r2 = cs[2];  // window, oldest first, kept as stored
     const float w0 = tof(q0), w1 = tof(q1), w2 = tof(q2), w3 = tof(q3);
-    T c0 = r0, c1 = r1, c2 = r2;  // window after row a
+    if (MODE == kDeferred) {  // the window after the previous call's rows: the one the slot commits
+#pragma unroll
+      for (int i = 0; i < kWS; ++i) {
+        if (off - kWS + i >= 0) {
+          r0 = r1;
+          r1 = r2;
+          r2 = xq[i];
+        }
+      }
+    }
+    T c0 = r0, c1 = r1, c2 = r2;  // window after row a (deferred: after the previous rows)
 #pragma unroll
     for (int t = 0; t < RMAX; ++t) {
-      if (t < t_end) {
+      if (t < n) {
         const T r3 = xr[t];
         float z = __fmul_rn(w0, tof(r0));
         z = __fmaf_rn(w1, tof(r1), z);
@@ -487,7 +526,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
           sc[1] = r1;
           sc[2] = r2;
         }
-        if (kCommits && t == a) {
+        if (kCommits && MODE != kDeferred && t == a) {
           c0 = r0;
           c1 = r1;
           c2 = r2;
@@ -500,12 +539,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
       cs[2] = c2;
     }
   }
+  if (n == 0) return;  // only the previous call's rows: the window was all there was to do
   __syncthreads();
   // Raw dot products of the rows' conv outputs, packed in n-row order: entries
   // e < n are q_t.q_t, then pairs (s, t) at n + 2 (s n + t) + {0: k_s.k_t,
   // 1: k_s.q_t}.  They give the L2 norms (diagonals) and, scaled, the Gram
   // tables.
-  const int n = t_end;
   const int nd = n + 2 * n * n;
   __shared__ float sdot[RMAX + 2 * RMAX * RMAX];
   if constexpr (RMAX <= 4) {
@@ -592,9 +631,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   __syncthreads();
   auto fq = [&](int t) { return __fmul_rn(p.scale, rsqrtf(__fadd_rn(sdot[t], p.eps))); };
   auto fk = [&](int t) { return rsqrtf(__fadd_rn(sdot[n + 2 * (t * n + t)], p.eps)); };
-  if (active) {  // publish scale*q^ | k^
+  if (active) {  // publish scale*q^ | k^ (and, deferred, k^ into the carry)
     float* dst = p.wqk + ((size_t)b * p.H_qk + hq) * p.R * 2 * DK + tid;
-    for (int t = 0; t < n; ++t) dst[(size_t)t * 2 * DK] = __fmul_rn(sy[t][tid], tid < DK ? fq(t) : fk(t));
+    float* kc = MODE == kDeferred && tid >= DK ? p.ck + ((size_t)b * p.H_qk + hq) * p.R * DK + (tid - DK) : nullptr;
+    for (int t = 0; t < n; ++t) {
+      const float v = __fmul_rn(sy[t][tid], tid < DK ? fq(t) : fk(t));
+      dst[(size_t)t * 2 * DK] = v;
+      if (kc != nullptr) kc[(size_t)t * DK] = v;
+    }
   }
   // Gram tables [R][R][2]: k^_s . k^_t and k^_s . (scale q^_t); rows past n are zero
   float* gh = p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(p.R);
@@ -606,16 +650,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     gh[i] = val;
   }
   // per-row decay and write strength of the value heads that read this q/k head
-  for (int i = tid; i < p.G * t_end; i += kPrepThreads) {
-    const int h = hq * p.G + i / t_end, t = i % t_end;
+  for (int i = tid; i < p.G * n; i += kPrepThreads) {
+    const int h = hq * p.G + i / n, t = i % n;
     if (i >= kPrepThreads) load_gate(t, h, g_i, beta_i);  // more (head, row) pairs than threads: load now
     float gg = g_i, bb = beta_i;
     if (p.raw_gating) {  // g = -exp(A_log) softplus(a), beta = sigmoid(b), overflow-free forms
       gg = -expf(__ldg(p.A_log + h)) * (fmaxf(g_i, 0.f) + log1pf(expf(-fabsf(g_i))));
       bb = 1.f / (1.f + expf(-beta_i));
     }
-    *reinterpret_cast<float4*>(p.wsc + (((size_t)b * p.H_v + h) * p.R + t) * 4) =
-        make_float4(expf(gg), bb, 0.f, 0.f);
+    const float decay = expf(gg);
+    *reinterpret_cast<float4*>(p.wsc + (((size_t)b * p.H_v + h) * p.R + t) * 4) = make_float4(decay, bb, 0.f, 0.f);
+    if (MODE == kDeferred) p.ca[((size_t)b * p.H_v + h) * round4(p.R) + t] = decay;
   }
 }
 
@@ -640,7 +685,11 @@ template <int DK>
 struct Stage {
   static constexpr int DVS = Geo<DK>::DVS;
   __host__ __device__ static int rows_floats(int R) { return R * 2 * DK + R * DVS + R * 4 + gram_floats(R); }
-  __host__ __device__ static size_t bytes(int R) { return sizeof(float) * ((size_t)DVS * DK + 2 * (size_t)rows_floats(R)); }
+  // deferred mode: a previous call's carry rows, [Rp][DVS] u | [Rp][DK] k^ | [Rp4] exp(g)
+  __host__ __device__ static int carry_floats(int Rp) { return Rp * DVS + Rp * DK + round4(Rp); }
+  __host__ __device__ static size_t bytes(int R, int Rp = 0) {
+    return sizeof(float) * ((size_t)DVS * DK + 2 * (size_t)(rows_floats(R) + carry_floats(Rp)));
+  }
 };
 
 // Sums, over the LPR lanes of a row group, each lane's partial dot products of
@@ -706,22 +755,26 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_items = p.B * p.H_v * p.slices;
   const int R = p.R;
-  const int rfl = Stage<DK>::rows_floats(R);
+  const int Rp = MODE == kDeferred ? p.Rp : 0;
+  const int rfl = Stage<DK>::rows_floats(R) + Stage<DK>::carry_floats(Rp);
   extern __shared__ __align__(16) float smem[];
   float* const stS = smem;  // [DVS][DK] state slice of the next item
   auto stQK = [&](int s) { return smem + DVS * DK + (size_t)s * rfl; };  // [R][2 DK]  scale*q^ | k^
   auto stV = [&](int s) { return stQK(s) + R * 2 * DK; };               // [R][DVS]   v
   auto stSC = [&](int s) { return stV(s) + R * DVS; };                  // [R][4]     exp(g), beta
   auto stGH = [&](int s) { return stSC(s) + R * 4; };                   // [R][R][2]  k.k, k.q~ (padded)
+  auto stCU = [&](int s) { return stGH(s) + gram_floats(R); };          // [Rp][DVS]  previous rows' u
+  auto stCK = [&](int s) { return stCU(s) + Rp * DVS; };                // [Rp][DK]   previous rows' k^
+  auto stCA = [&](int s) { return stCK(s) + Rp * DK; };                 // [Rp4]      previous rows' exp(g)
   __shared__ __align__(8) uint64_t barS, barQ[2];
-  __shared__ int sMeta[2][4];  // per item parity: slot, rows to run, commit row (-1 none), previous rows
+  __shared__ int sMeta[2][4];  // per item parity: slot, rows to run, commit row (-1 none), previous rows to commit
 
   // ---- producer side (thread 0) ----
   // An item's request data is loaded one item ahead of its use and evaluated
   // only when its copies are issued, so the producer's warp never waits on
   // those loads while the item before it computes.
   struct Req {
-    int n, slot, a, np;  // np: the previous step's rows (deferred mode), a then its accepted drafts
+    int n, slot, a, np;  // np: the previous call's rows (deferred mode), a then its accepted drafts
   };
   auto load_req = [&](int it) {
     const int b = it / (p.H_v * p.slices);
@@ -742,9 +795,10 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const int hs = it % (p.H_v * p.slices);
     int report, crow, off = 0;
     m[0] = q.slot;
-    if (MODE == kDeferred)
-      m[1] = deferred_rows_of(p, q.n, q.slot, q.np, q.a, off, crow, report);
-    else
+    if (MODE == kDeferred) {  // rows = the current rows only; off previous rows are committed first
+      const int t_end = deferred_rows_of(p, q.n, q.slot, q.np, q.a, off, crow, report);
+      m[1] = t_end - off;
+    } else
       m[1] = request_rows_of<kCommits, MODE == kCommitReplay>(p, q.n, q.slot, q.a, crow, report);
     m[2] = crow;
     m[3] = off;
@@ -760,8 +814,11 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     mbar_expect_tx(&barS, kSBytes);
     bulk_load(stS, p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS);
   };
-  auto issue_rows = [&](int s, int it, int rows) {
-    if (rows == 0) {
+  // rows: current rows to stage; prev: previous rows whose carry is staged (deferred mode)
+  auto issue_rows = [&](int s, int it, int rows, int prev) {
+    const uint32_t rb = rows > 0 ? (rows * (2 * DK + DVS + 4) + gram_floats(R)) * sizeof(float) : 0;
+    const uint32_t cb = prev > 0 ? (prev * (DVS + DK) + round4(prev)) * sizeof(float) : 0;
+    if (rb + cb == 0) {
       mbar_arrive(&barQ[s]);
       return;
     }
@@ -769,12 +826,20 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const int hs = it - b * p.H_v * p.slices;
     const int h = hs / p.slices;
     const int hq = h / p.G;
-    mbar_expect_tx(&barQ[s], (uint32_t)((rows * (2 * DK + DVS + 4) + gram_floats(R)) * sizeof(float)));
-    bulk_load(stQK(s), p.wqk + ((size_t)b * p.H_qk + hq) * R * 2 * DK, rows * 2 * DK * sizeof(float), &barQ[s]);
-    bulk_load(stV(s), p.wv + ((size_t)b * p.H_v * p.slices + hs) * R * DVS, rows * DVS * sizeof(float), &barQ[s]);
-    bulk_load(stSC(s), p.wsc + ((size_t)b * p.H_v + h) * R * 4, rows * 4 * sizeof(float), &barQ[s]);
-    bulk_load(stGH(s), p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(R), gram_floats(R) * sizeof(float),
-              &barQ[s]);
+    mbar_expect_tx(&barQ[s], rb + cb);
+    if (rows > 0) {
+      bulk_load(stQK(s), p.wqk + ((size_t)b * p.H_qk + hq) * R * 2 * DK, rows * 2 * DK * sizeof(float), &barQ[s]);
+      bulk_load(stV(s), p.wv + ((size_t)b * p.H_v * p.slices + hs) * R * DVS, rows * DVS * sizeof(float), &barQ[s]);
+      bulk_load(stSC(s), p.wsc + ((size_t)b * p.H_v + h) * R * 4, rows * 4 * sizeof(float), &barQ[s]);
+      bulk_load(stGH(s), p.wgh + ((size_t)b * p.H_qk + hq) * gram_floats(R), gram_floats(R) * sizeof(float),
+                &barQ[s]);
+    }
+    if (MODE == kDeferred && prev > 0) {
+      bulk_load(stCU(s), p.pcu + ((size_t)b * p.H_v * p.slices + hs) * Rp * DVS, prev * DVS * sizeof(float),
+                &barQ[s]);
+      bulk_load(stCK(s), p.pck + ((size_t)b * p.H_qk + hq) * Rp * DK, prev * DK * sizeof(float), &barQ[s]);
+      bulk_load(stCA(s), p.pca + ((size_t)b * p.H_v + h) * round4(Rp), round4(prev) * sizeof(float), &barQ[s]);
+    }
   };
 
   // Two producer threads, one per warp, so each warp issues part of the next
@@ -793,12 +858,12 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       const Req q0 = load_req(blockIdx.x);
       if (blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);  // both in flight
       meta(blockIdx.x, q0, sMeta[0]);
-      issue_state(blockIdx.x, sMeta[0][0], sMeta[0][1]);  // before the prologue has finished
+      issue_state(blockIdx.x, sMeta[0][0], sMeta[0][1] + sMeta[0][3]);  // before the prologue has finished
     }
   }
   __syncthreads();  // the barriers are initialised before anyone waits on them
   pdl_wait();       // the prologue's q, k, v and tables are complete and visible
-  if (tid == kRowsProducer && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1]);
+  if (tid == kRowsProducer && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1], sMeta[0][3]);
 
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
@@ -820,11 +885,13 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       mbar_wait(&barQ[s], (k >> 1) & 1);
       return;
     }
-    const int slot = sMeta[s][0], rows = sMeta[s][1], a = sMeta[s][2];
-    const int off = MODE == kDeferred ? sMeta[s][3] : 0;  // leading rows that are the previous step's
+    const int slot = sMeta[s][0], rows = sMeta[s][1];
+    const int prev = MODE == kDeferred ? sMeta[s][3] : 0;  // previous call's rows to commit first
+    const int a = MODE == kDeferred ? -1 : sMeta[s][2];    // commit row among this call's rows
+    const bool busy = rows > 0 || prev > 0;
 
     f2 S[M][NP];  // column pairs of the lane's 4-column chunks
-    if (rows > 0) {
+    if (busy) {
 #pragma unroll
       for (int m = 0; m < M; ++m)
 #pragma unroll
@@ -847,13 +914,13 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         if (tid == 0) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) sMeta[s ^ 1][j] = m[j];
-          issue_state(it1, m[0], m[1]);
+          issue_state(it1, m[0], m[1] + m[3]);
         }
-        if (tid == kRowsProducer) issue_rows(s ^ 1, it1, m[1]);
+        if (tid == kRowsProducer) issue_rows(s ^ 1, it1, m[1], m[3]);
         if (it1 + gridDim.x < n_items) qn = load_req(it1 + gridDim.x);  // in flight while this item computes
       }
     }
-    if (rows == 0) continue;
+    if (!busy) continue;
 
     const int b = it / (p.H_v * p.slices);
     const int hs = it - b * p.H_v * p.slices;
@@ -864,11 +931,11 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const float* sGH = stGH(s);
     float* Sg = p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK;
     float* og = nullptr;
-    if (kWantO) og = p.o + ((size_t)b * p.Rc * p.H_v + h) * p.d_v + (size_t)sl * DVS + rl;
+    if (kWantO) og = p.o + ((size_t)b * p.R * p.H_v + h) * p.d_v + (size_t)sl * DVS + rl;
 
-    // lane's column pairs of row vector t (q at offset 0, k at offset DK)
-    auto load_vec = [&](int t, int off, f2 (&vv)[NP]) {
-      const ulonglong2* vp = reinterpret_cast<const ulonglong2*>(sQK + t * 2 * DK + off);
+    // lane's column pairs of the d_k-vector at rp
+    auto load_row = [&](const float* rp, f2 (&vv)[NP]) {
+      const ulonglong2* vp = reinterpret_cast<const ulonglong2*>(rp);
 #pragma unroll
       for (int j = 0; j < NC4; ++j) {
         const ulonglong2 v = vp[c + LPR * j];
@@ -876,8 +943,12 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         vv[2 * j + 1] = v.y;
       }
     };
-    // dst[m] = cc * S[m] + sum_{s<nt} w_s(row m) k_{c0+s}, in that order; in place when dst is S
-    auto combine = [&](int c0, int nt, float cc, const float (&w)[CH], bool in_place, float* out) {
+    // row vector t of the item's rows: q at part 0, k at part DK
+    auto load_vec = [&](int t, int part, f2 (&vv)[NP]) { load_row(sQK + t * 2 * DK + part, vv); };
+    // dst[m] = cc * S[m] + sum_{x<nt} w_x(row m) k_x, k_x the d_k-vector at kb + x ks, in that order;
+    // in place when dst is S
+    auto combine = [&](const float* kb, int ks, int nt, float cc, const float (&w)[CH], bool in_place,
+                       float* out) {
       // coefficient x of row m lives in the lane holding row m's sums
       auto wm = [&](int m, int x) { return __shfl_sync(kFull, w[x], gbase | lane_of_row<LPR, M>(m)); };
       const f2 cc2 = pack2(cc, cc);
@@ -890,7 +961,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         for (int x = 0; x < CH; ++x) {
           if (x < nt) {
             f2 kv[NP];
-            load_vec(c0 + x, DK, kv);
+            load_row(kb + x * ks, kv);
 #pragma unroll
             for (int m = 0; m < M; ++m) {
               const float wx = wm(m, x);
@@ -910,7 +981,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
           for (int x = 0; x < CH; ++x) {
             if (x < nt) {
               f2 kv[NP];
-              load_vec(c0 + x, DK, kv);
+              load_row(kb + x * ks, kv);
               const float wx = wm(m, x);
               const f2 w2 = pack2(wx, wx);
 #pragma unroll
@@ -932,6 +1003,31 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
           *reinterpret_cast<ulonglong2*>(out + (size_t)(wrow + m * RG) * DK + 4 * (c + LPR * j)) =
               make_ulonglong2(S[m][2 * j], S[m][2 * j + 1]);
     };
+
+    // ---- deferred: commit the previous call's rows 0..prev-1 from its carry ----
+    //   S <- C S + sum_{s<prev} (u_s prod_{s<j<prev} alpha_j) k_s^T,  C = prod_{j<prev} alpha_j
+    if (MODE == kDeferred && prev > 0) {
+      const float* sCU = stCU(s);
+      const float* sCK = stCK(s);
+      const float* sCA = stCA(s);
+      float ctot = 1.f;
+      for (int j = 0; j < prev; ++j) ctot = __fmul_rn(ctot, sCA[j]);
+      for (int s0 = 0; s0 < prev; s0 += CH) {
+        float w[CH];
+#pragma unroll
+        for (int x = 0; x < CH; ++x) {
+          const int sx = s0 + x;
+          float d = 0.f;
+          if (sx < prev) {
+            d = sCU[sx * DVS + rl];
+            for (int j = sx + 1; j < prev; ++j) d = __fmul_rn(d, sCA[j]);
+          }
+          w[x] = d;
+        }
+        combine(sCK + s0 * DK, DK, prev - s0 < CH ? prev - s0 : CH, s0 == 0 ? ctot : 1.f, w, true, nullptr);
+      }
+      store_state(Sg);
+    }
 
     for (int c0 = 0; c0 < rows; c0 += CH) {
       const int nc = rows - c0 < CH ? rows - c0 : CH;
@@ -999,12 +1095,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
               r = __fmaf_rn(z[x], sGH[((c0 + x) * R + (c0 + t)) * 2], r);
             }
           z[t] = __fmul_rn(ab.y, __fsub_rn(sV[(c0 + t) * DVS + rl], r));
+          if (MODE == kDeferred && writer)  // the row's update vector, for the next call's commit
+            p.cu[(((size_t)b * p.H_v * p.slices + hs) * R + c0 + t) * DVS + rl] = z[t];
           if constexpr (kWantO) {
             float oo = __fmul_rn(cdec, pq[t]);
 #pragma unroll
             for (int x = 0; x < CH; ++x)
               if (x <= t) oo = __fmaf_rn(z[x], sGH[((c0 + x) * R + (c0 + t)) * 2 + 1], oo);
-            if (writer && (MODE != kDeferred || c0 + t >= off)) og[(size_t)(c0 + t - off) * o_tstride] = oo;
+            if (writer) og[(size_t)(c0 + t) * o_tstride] = oo;
           }
           if (kCommits && c0 + t == a) {
 #pragma unroll
@@ -1013,21 +1111,21 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
             ncom = t + 1;
           }
           if (kSnap)
-            combine(c0, t + 1, cdec, z, false,
+            combine(sQK + c0 * 2 * DK + DK, 2 * DK, t + 1, cdec, z, false,
                     p.snapS + (((size_t)b * R + c0 + t) * p.H_v * p.slices + hs) * DVS * DK);
         }
       }
       // ---- commit: S_a = C_a S0 + sum_{s<=a} z_s k_s^T ----
       if (kCommits && ncom > 0) {
         if (last) {
-          combine(c0, ncom, ccom, zc, true, nullptr);
+          combine(sQK + c0 * 2 * DK + DK, 2 * DK, ncom, ccom, zc, true, nullptr);
           store_state(Sg);
         } else {
-          combine(c0, ncom, ccom, zc, false, Sg);
+          combine(sQK + c0 * 2 * DK + DK, 2 * DK, ncom, ccom, zc, false, Sg);
         }
       }
       // ---- advance the state to the chunk's end when rows follow ----
-      if (!last) combine(c0, nc, cdec, z, true, nullptr);
+      if (!last) combine(sQK + c0 * 2 * DK + DK, 2 * DK, nc, cdec, z, true, nullptr);
     }
   }
   pdl_trigger();  // CTAs that had no item
@@ -1089,7 +1187,7 @@ int prefer_max_shared(Kernel kernel) {
 template <int DK, int MODE>
 int launch_rows(const Params& p, cudaStream_t st) {
   using Gm = Geo<DK>;
-  const size_t smem = Stage<DK>::bytes(p.R);
+  const size_t smem = Stage<DK>::bytes(p.R, MODE == kDeferred ? p.Rp : 0);
   struct Cache {
     int dev = -1;
     size_t smem = 0;
@@ -1269,21 +1367,22 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.raw_gating = (a->flags & GDN_FLAG_RAW_GATING) != 0;
   p.A_log = p.raw_gating ? a->A_log : nullptr;
   p.xp = nullptr;
-  p.gp = p.betap = nullptr;
   p.n_prev = p.acc_prev = nullptr;
+  p.pcu = p.pck = p.pca = nullptr;
+  p.cu = p.ck = p.ca = nullptr;
   p.Rp = 0;
-  p.Rc = a->R;
   return GDN_OK;
 }
 
-// The deferred call's shape: the current step's arguments with R widened by
-// the previous step's rows, which is how the work buffer is sized.
-int deferred_shape(const gdn_args* cur, int prev_R, gdn_args* out) {
-  if (!cur || prev_R < 0) return GDN_ERR_INVALID_ARG;
-  if (cur->R < 1) return GDN_ERR_INVALID_ARG;
-  *out = *cur;
-  out->R = cur->R + prev_R;
-  return check_shape(out);
+// Carry of a deferred call with R rows per request:
+//   u [B][H_v d_v / dvs][R][dvs], k^ [B][H_qk][R][d_k], exp(g) [B][H_v][R4]
+// (R4 = R rounded up to 4).  Every region starts on 16 bytes.
+size_t carry_floats(const gdn_args* a, int R, size_t* off_k, size_t* off_a) {
+  const size_t u = (size_t)a->B * R * a->H_v * a->d_v;
+  const size_t k = (size_t)a->B * R * a->H_qk * a->d_k;
+  if (off_k) *off_k = u;
+  if (off_a) *off_a = u + k;
+  return u + k + (size_t)a->B * a->H_v * round4(R);
 }
 
 int run_rows(const gdn_args* args, unsigned need, int mode, void* stream) {
@@ -1304,27 +1403,36 @@ int run_rows(const gdn_args* args, unsigned need, int mode, void* stream) {
 }
 
 int run_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream) {
-  const int prev_R = prev ? prev->R : 0;
-  if (prev && prev->R < 1) return GDN_ERR_INVALID_ARG;
-  gdn_args a;
-  int rc = deferred_shape(cur, prev_R, &a);
+  int rc = check_shape(cur);
   if (rc != GDN_OK) return rc;
+  if (prev != nullptr) {
+    if (prev->R < 1) return GDN_ERR_INVALID_ARG;
+    if (prev->R > kMaxR) return GDN_ERR_UNSUPPORTED;
+  }
   Params p;
-  rc = validate(&a, kNeedRows | kNeedO, &p);
+  rc = validate(cur, kNeedRows | kNeedO, &p);
   if (rc != GDN_OK) return rc;
-  if (prev) {
-    if (!prev->x || !prev->g || !prev->beta || !prev->n_rows || !prev->accept_len) return GDN_ERR_INVALID_ARG;
-    if (!aligned(prev->x, 16) || !aligned(prev->g, 4) || !aligned(prev->beta, 4) || !aligned(prev->n_rows, 4) ||
-        !aligned(prev->accept_len, 4))
+  if (!cur->carry) return GDN_ERR_INVALID_ARG;
+  if (!aligned(cur->carry, 16)) return GDN_ERR_MISALIGNED;
+  size_t ok = 0, oa = 0;
+  carry_floats(cur, cur->R, &ok, &oa);
+  p.cu = static_cast<float*>(cur->carry);
+  p.ck = p.cu + ok;
+  p.ca = p.cu + oa;
+  if (prev != nullptr) {
+    if (!prev->x || !prev->n_rows || !prev->accept_len || !prev->carry) return GDN_ERR_INVALID_ARG;
+    if (!aligned(prev->x, 16) || !aligned(prev->n_rows, 4) || !aligned(prev->accept_len, 4) ||
+        !aligned(prev->carry, 16))
       return GDN_ERR_MISALIGNED;
+    carry_floats(cur, prev->R, &ok, &oa);
+    p.pcu = static_cast<const float*>(prev->carry);
+    p.pck = p.pcu + ok;
+    p.pca = p.pcu + oa;
     p.xp = prev->x;
-    p.gp = prev->g;
-    p.betap = prev->beta;
     p.n_prev = prev->n_rows;
     p.acc_prev = prev->accept_len;
+    p.Rp = prev->R;
   }
-  p.Rp = prev_R;
-  p.Rc = cur->R;
   if (p.B == 0) return GDN_OK;
   return run_mode<kDeferred>(p, cur->in_dtype, static_cast<cudaStream_t>(stream));
 }
@@ -1365,10 +1473,9 @@ GDN_API int gdn_verify_commit(const gdn_args* args, void* stream) {
   return run_rows(args, kNeedRows | kNeedO | kNeedAccept, kFused, stream);
 }
 
-GDN_API size_t gdn_deferred_work_bytes(const gdn_args* cur, int prev_R) {
-  gdn_args a;
-  if (deferred_shape(cur, prev_R, &a) != GDN_OK) return 0;
-  return sizeof(float) * work_floats(&a, nullptr, nullptr, nullptr);
+GDN_API size_t gdn_carry_bytes(const gdn_args* args) {
+  if (check_shape(args) != GDN_OK) return 0;
+  return sizeof(float) * carry_floats(args, args->R, nullptr, nullptr);
 }
 
 GDN_API int gdn_verify_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream) {

@@ -32,7 +32,7 @@ class GdnArgs(ctypes.Structure):
         ("flags", _I32),
         ("x", _P), ("g", _P), ("beta", _P), ("conv_w", _P), ("conv_state", _P), ("ssm_state", _P),
         ("slot_ids", _P), ("n_rows", _P), ("accept_len", _P), ("o", _P), ("scratch_S", _P),
-        ("scratch_cs", _P), ("work", _P), ("status", _P), ("A_log", _P),
+        ("scratch_cs", _P), ("work", _P), ("status", _P), ("A_log", _P), ("carry", _P),
     ]
 
 
@@ -73,13 +73,13 @@ _lib.gdn_greedy_accept.restype = ctypes.c_int
 class GdnPrevRows(ctypes.Structure):
     """Mirror of ``gdn_prev_rows``: the pending rows of a deferred commit."""
 
-    _fields_ = [("R", _I32), ("x", _P), ("g", _P), ("beta", _P), ("n_rows", _P), ("accept_len", _P)]
+    _fields_ = [("R", _I32), ("x", _P), ("n_rows", _P), ("accept_len", _P), ("carry", _P)]
 
 
 _lib.gdn_verify_deferred.argtypes = [ctypes.POINTER(GdnArgs), ctypes.POINTER(GdnPrevRows), _P]
 _lib.gdn_verify_deferred.restype = ctypes.c_int
-_lib.gdn_deferred_work_bytes.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_int]
-_lib.gdn_deferred_work_bytes.restype = ctypes.c_size_t
+_lib.gdn_carry_bytes.argtypes = [ctypes.POINTER(GdnArgs)]
+_lib.gdn_carry_bytes.restype = ctypes.c_size_t
 
 
 def strerror(code: int) -> str:
@@ -127,28 +127,29 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
-def make_prev(*, x, g, beta, n_rows, accept_len) -> GdnPrevRows:
-    """The previous step's pending rows for ``gdn_verify_deferred``: x
-    [B][R][C], g and beta [B][R][H_v], n_rows and accept_len [B]."""
-    return GdnPrevRows(R=x.shape[1], x=_ptr(x), g=_ptr(g), beta=_ptr(beta), n_rows=_ptr(n_rows),
-                       accept_len=_ptr(accept_len))
+def make_prev(*, x, n_rows, accept_len, carry) -> GdnPrevRows:
+    """The previous call's pending rows for ``gdn_verify_deferred``: its x
+    [B][R][C], n_rows and accept_len [B], and the carry it wrote."""
+    return GdnPrevRows(R=x.shape[1], x=_ptr(x), n_rows=_ptr(n_rows), accept_len=_ptr(accept_len),
+                       carry=_ptr(carry))
 
 
-def deferred_work_bytes(args: GdnArgs, prev_R: int) -> int:
-    """Scratch bytes of a deferred call with prev_R pending rows per request."""
-    return int(_lib.gdn_deferred_work_bytes(ctypes.byref(args), prev_R))
+def carry_bytes(args: GdnArgs) -> int:
+    """Bytes of carry a deferred call with these shapes writes (0 if the shapes are invalid)."""
+    return int(_lib.gdn_carry_bytes(ctypes.byref(args)))
 
 
 def gdn_verify_deferred(args: GdnArgs, prev: GdnPrevRows | None, stream=None) -> None:
-    """Commit the previous step's accepted rows and verify the current ones in
-    one pass (``gdn_verify_deferred``); prev None = nothing pending."""
+    """Commit the previous call's accepted rows (from its carry) and verify the
+    current ones in one pass (``gdn_verify_deferred``); prev None = nothing
+    pending.  args.carry receives this call's carry."""
     _check(_lib.gdn_verify_deferred(ctypes.byref(args), None if prev is None else ctypes.byref(prev),
                                     _stream(stream)), "gdn_verify_deferred")
 
 
 def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_qk: int,
               accept_len=None, o=None, scratch_S=None, scratch_cs=None, work=None,
-              status=None, scale: float | None = None, l2_eps: float = 1e-6, A_log=None) -> GdnArgs:
+              status=None, scale: float | None = None, l2_eps: float = 1e-6, A_log=None, carry=None) -> GdnArgs:
     """Fill a GdnArgs from tensors laid out as ``include/gdnspec.h`` states.
 
     Shapes are read from x [B][R][C], ssm_state [P][H_v][d_v][d_k] and
@@ -171,7 +172,8 @@ def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_
         x=_ptr(x), g=_ptr(g), beta=_ptr(beta), conv_w=_ptr(conv_w), conv_state=_ptr(conv_state),
         ssm_state=_ptr(ssm_state), slot_ids=_ptr(slot_ids), n_rows=_ptr(n_rows),
         accept_len=_ptr(accept_len), o=_ptr(o), scratch_S=_ptr(scratch_S),
-        scratch_cs=_ptr(scratch_cs), work=_ptr(work), status=_ptr(status), A_log=_ptr(A_log))
+        scratch_cs=_ptr(scratch_cs), work=_ptr(work), status=_ptr(status), A_log=_ptr(A_log),
+        carry=_ptr(carry))
 
 
 class DeviceLayer:

@@ -224,18 +224,20 @@ def spec_bytes(spec: LayerSpec, n_rows) -> int:
 
 def deferred_bytes(spec: LayerSpec, n_rows, n_prev, acc_prev) -> int:
     """Algorithmic bytes of one deferred-commit call: ``spec_bytes``'s terms
-    for every request with current or pending rows, plus the pending rows' x,
-    g and beta (acc_prev + 1 rows of each request with pending rows)."""
+    for every request with current or pending rows; for a request with
+    pending rows, those rows' x (acc_prev + 1 rows, for the conv window) and
+    their carry (per row: H_v d_v update values, H_qk d_k of k^, H_v decays)
+    read; and the carry of the current rows written."""
     s = 2 * spec.H_v * spec.d_v * spec.d_k * 4
     cs = 2 * spec.C * (spec.W - 1) * spec.elem_bytes
     per_row = spec.C * spec.elem_bytes + spec.H_v * 8 + spec.H_v * spec.d_v * 4
-    pending_row = spec.C * spec.elem_bytes + spec.H_v * 8
+    carry_row = (spec.H_v * spec.d_v + spec.H_qk * spec.d_k + spec.H_v) * 4
     total = spec.C * spec.W * spec.elem_bytes
     for n, np_, a in zip((int(v) for v in n_rows), (int(v) for v in n_prev), (int(v) for v in acc_prev)):
         if n > 0 or np_ > 0:
-            total += s + cs + max(n, 0) * per_row
+            total += s + cs + max(n, 0) * (per_row + carry_row)
         if np_ > 0:
-            total += (a + 1) * pending_row
+            total += (a + 1) * (spec.C * spec.elem_bytes + carry_row)
     return total
 
 

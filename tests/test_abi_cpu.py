@@ -22,7 +22,7 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     assert set(declared_symbols()) == {"gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_work_bytes",
                                       "gdn_strerror", "gdn_verify_commit_static", "gdn_greedy_accept",
-                                      "gdn_verify_deferred", "gdn_deferred_work_bytes"}
+                                      "gdn_verify_deferred", "gdn_carry_bytes"}
 
 
 def test_library_exports_every_declared_symbol(cuda_lib):
@@ -192,7 +192,7 @@ def test_greedy_accept_empty_batch_is_a_no_op(cuda_lib):
 
 
 def good_prev(gdn, **over):
-    p = gdn.GdnPrevRows(R=4, x=FAKE, g=FAKE, beta=FAKE, n_rows=FAKE, accept_len=FAKE)
+    p = gdn.GdnPrevRows(R=4, x=FAKE, n_rows=FAKE, accept_len=FAKE, carry=FAKE)
     for k, v in over.items():
         setattr(p, k, v)
     return p
@@ -200,11 +200,15 @@ def good_prev(gdn, **over):
 
 DEFERRED_CASES = [
     ("zero pending rows", dict(), dict(R=0), 1),
-    ("rows over 16 in all", dict(R=9), dict(R=8), 2),
+    ("pending rows over 16", dict(), dict(R=17), 2),
     ("null pending x", dict(), dict(x=None), 1),
     ("null pending accept_len", dict(), dict(accept_len=None), 1),
+    ("null pending carry", dict(), dict(carry=None), 1),
     ("misaligned pending x", dict(), dict(x=FAKE + 2), 3),
     ("misaligned pending n_rows", dict(), dict(n_rows=FAKE + 1), 3),
+    ("misaligned pending carry", dict(), dict(carry=FAKE + 4), 3),
+    ("null carry out", dict(carry=None), dict(), 1),
+    ("misaligned carry out", dict(carry=FAKE + 8), dict(), 3),
     ("null o", dict(o=None), dict(), 1),
     ("null work", dict(work=None), dict(), 1),
     ("d_k", dict(d_k=96), dict(), 2),
@@ -213,26 +217,25 @@ DEFERRED_CASES = [
 
 @pytest.mark.parametrize("what,cur,prev,code", DEFERRED_CASES, ids=[c[0] for c in DEFERRED_CASES])
 def test_deferred_rejects_bad_arguments(cuda_lib, what, cur, prev, code):
-    a, p = good_args(cuda_lib, **cur), good_prev(cuda_lib, **prev)
+    a, p = good_args(cuda_lib, **{"carry": FAKE, **cur}), good_prev(cuda_lib, **prev)
     rc = cuda_lib._lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(p), None)
     assert rc == code, (what, cuda_lib.strerror(rc))
 
 
 def test_deferred_empty_batch_and_no_pending_rows(cuda_lib):
     lib, g = cuda_lib._lib, cuda_lib
-    a = good_args(g, B=0, accept_len=None)  # the deferred call never reads accept_len
+    a = good_args(g, B=0, accept_len=None, carry=FAKE)  # the deferred call never reads accept_len
     assert lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(good_prev(g)), None) == g.OK
     assert lib.gdn_verify_deferred(ctypes.byref(a), None, None) == g.OK
     assert lib.gdn_verify_deferred(None, None, None) == g.ERR_INVALID_ARG
-    a = good_args(g, R=16)  # 16 current rows leave no room for a pending row
+    a = good_args(g, R=17, carry=FAKE)
     assert lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(good_prev(g, R=1)), None) == g.ERR_UNSUPPORTED
 
 
-def test_deferred_work_bytes(cuda_lib):
-    a = good_args(cuda_lib, R=3)
-    wide = good_args(cuda_lib, R=3 + 4)
-    assert cuda_lib.deferred_work_bytes(a, 4) == cuda_lib.work_bytes(wide) > cuda_lib.work_bytes(a)
-    assert cuda_lib.deferred_work_bytes(a, 0) == cuda_lib.work_bytes(a)
-    assert cuda_lib.deferred_work_bytes(a, -1) == 0
-    assert cuda_lib.deferred_work_bytes(a, 14) == 0  # 17 rows
-    assert cuda_lib._lib.gdn_deferred_work_bytes(None, 1) == 0
+def test_carry_bytes(cuda_lib):
+    B, R, Hq, Hv, dk, dv = 2, 3, 16, 32, 128, 128
+    a = good_args(cuda_lib, R=R)
+    assert cuda_lib.carry_bytes(a) == 4 * (B * R * (Hv * dv + Hq * dk) + B * Hv * 4)
+    assert cuda_lib.carry_bytes(good_args(cuda_lib, R=5)) == 4 * (B * 5 * (Hv * dv + Hq * dk) + B * Hv * 8)
+    assert cuda_lib.carry_bytes(good_args(cuda_lib, d_k=96)) == 0
+    assert cuda_lib._lib.gdn_carry_bytes(None) == 0

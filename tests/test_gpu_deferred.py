@@ -32,25 +32,29 @@ def _gpu(cuda_lib):
 
 
 def run_deferred(cur, prev, raw_gating=False):
-    """One deferred call on the GPU.  Returns (DeviceLayer after the call,
-    tensors kept alive)."""
+    """Two deferred calls on the GPU sharing one slot pool: the previous
+    step's (nothing pending; it writes its carry), then the current step's,
+    which commits the previous step's accepted rows from that carry.  Returns
+    (DeviceLayer of the current call, DeviceLayer of the previous call)."""
     from speculative_decode_gateddeltanet_gb300 import gdn
 
     dev = gdn.DeviceLayer(cur, "cuda", raw_gating=raw_gating)
-    a = dev.args()
-    keep, pd = [], None
+    pd, pdev = None, None
     if prev is not None:
-        g_key, b_key = ("a_raw", "b_raw") if raw_gating else ("g", "beta")
-        t = {k: prev[v].cuda().contiguous() for k, v in
-             (("x", "x"), ("g", g_key), ("beta", b_key), ("n_rows", "n_rows"), ("accept_len", "accept_len"))}
-        pd = gdn.make_prev(**t)
-        keep.append(t)
-    work = torch.empty(gdn.deferred_work_bytes(a, pd.R if pd else 0) // 4, device="cuda")
-    a.work = work.data_ptr()
+        pdev = gdn.DeviceLayer(prev, "cuda", raw_gating=raw_gating)
+        pdev.conv_state, pdev.ssm_state = dev.conv_state, dev.ssm_state  # one pool
+        a1 = pdev.args()
+        pdev.carry = torch.empty(gdn.carry_bytes(a1) // 4, device="cuda")
+        a1.carry = pdev.carry.data_ptr()
+        gdn.gdn_verify_deferred(a1, None)
+        pd = gdn.make_prev(x=pdev.x, n_rows=pdev.n_rows, accept_len=pdev.accept_len, carry=pdev.carry)
+    a = dev.args()
+    dev.carry = torch.empty(gdn.carry_bytes(a) // 4, device="cuda")
+    a.carry = dev.carry.data_ptr()
     a.accept_len = None  # never read by the deferred call
     gdn.gdn_verify_deferred(a, pd)
     torch.cuda.synchronize()
-    return dev, keep
+    return dev, pdev
 
 
 def valid_current(cur, prev):
@@ -114,9 +118,15 @@ def test_deferred_matches_oracle(name, ps, cs):
     prev = make_layer(ps, 500 + len(name))
     cur = make_step(prev, cs, 600 + len(name))
     ref = oracle.verify_deferred(cur, prev)
-    dev, _ = run_deferred(cur, prev)
+    dev, pdev = run_deferred(cur, prev)
     assert int(dev.status.item()) == ref["status"] == 0
     check(cur, prev, dev, ref)
+    # the first call, with nothing pending, is a verify of the previous step's rows
+    first = oracle.verify_commit(prev, commit=False)
+    valid, _ = valid_current(prev, None)
+    o1 = pdev.o.double().cpu().numpy()
+    err = float(np.abs(o1[valid] - first["o"][valid]).max() / np.abs(first["o"][valid]).max())
+    assert err <= O_TOL and int(pdev.status.item()) == 0
 
 
 def test_deferred_raw_gating():
@@ -141,8 +151,9 @@ def test_nothing_pending_equals_verify_bitwise():
 
 def test_sequence_of_deferred_steps_matches_fused_steps():
     """Four decode steps in deferred form plus a flush, on the same device
-    buffers, against the oracle running each step as a fused verify+commit:
-    every step's o and the final pools."""
+    pools, each call committing the one before from its carry, against the
+    oracle running each step as a fused verify+commit: every step's o and the
+    final pools."""
     from speculative_decode_gateddeltanet_gb300 import gdn
 
     steps = [make_layer(spec_of(8, 3, inactive_frac=0.125), 90)]
@@ -166,9 +177,12 @@ def test_sequence_of_deferred_steps_matches_fused_steps():
         a = gdn.make_args(x=cur_t["x"], g=cur_t["g"], beta=cur_t["beta"], conv_w=conv_w,
                           conv_state=conv_state, ssm_state=ssm_state, slot_ids=slots,
                           n_rows=cur_t["n_rows"], o=o, status=status, H_qk=16)
-        pd = None if prev_t is None else gdn.make_prev(**prev_t)
-        work = torch.empty(gdn.deferred_work_bytes(a, pd.R if pd else 0) // 4, device="cuda")
+        cur_t["carry"] = torch.empty(gdn.carry_bytes(a) // 4, device="cuda")
+        a.carry = cur_t["carry"].data_ptr()
+        work = torch.empty(gdn.work_bytes(a) // 4, device="cuda")
         a.work = work.data_ptr()
+        pd = None if prev_t is None else gdn.make_prev(x=prev_t["x"], n_rows=prev_t["n_rows"],
+                                                       accept_len=prev_t["accept_len"], carry=prev_t["carry"])
         gdn.gdn_verify_deferred(a, pd)
         torch.cuda.synchronize()
         if not flush:  # the oracle's fused step i: o from the committed pools, then the commit
