@@ -287,7 +287,7 @@ __device__ __forceinline__ int deferred_rows_of(const Params& p, int n, int slot
 }
 // Request b's block of rows as every kernel of a call in mode MODE reads it:
 // rows to run; slot; crow = commit row (-1 none); off = leading rows that
-// are the previous step's (deferred mode; else 0); report = status bit.
+// are the previous call's (deferred mode; else 0); report = status bit.
 template <int MODE>
 __device__ __forceinline__ int request_block(const Params& p, int b, int& slot, int& crow, int& off, int& report) {
   slot = p.slot_ids[b];
