@@ -53,11 +53,11 @@ constexpr int kW = 4;             // conv width the kernels are built for
 constexpr int kWS = kW - 1;       // conv-state columns
 constexpr int kMaxR = 16;         // rows per request (k <= 15)
 constexpr int kPrepThreads = 256; // channels per prologue block (>= 2 * max d_k)
-// value channels per prologue thread: four (one chunk load per row) when a
-// request has at most 4 rows; with more rows the extra registers would cost
-// more resident blocks than the wider loads gain
+// value channels per prologue thread, loaded as one chunk per row: four when
+// a request has at most 4 rows, else two (four would cost more resident
+// blocks in registers than the wider loads gain)
 template <int RMAX>
-__host__ __device__ constexpr int vec_v() { return RMAX <= 4 ? 4 : 1; }
+__host__ __device__ constexpr int vec_v() { return RMAX <= 4 ? 4 : 2; }
 constexpr unsigned kFull = 0xffffffffu;
 
 // kDeferred: the previous call's accepted rows are committed from its carry
@@ -170,6 +170,14 @@ struct ChunkOf<float, 4> {
 template <>
 struct ChunkOf<__nv_bfloat16, 4> {
   using type = uint2;
+};
+template <>
+struct ChunkOf<float, 2> {
+  using type = float2;
+};
+template <>
+struct ChunkOf<__nv_bfloat16, 2> {
+  using type = uint32_t;
 };
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, __fadd_rn(1.0f, __expf(-z))); }
 
@@ -449,6 +457,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
         float* vd = vdst + (size_t)t * p.dvs;
         if constexpr (VV == 4)
           *reinterpret_cast<float4*>(vd) = make_float4(y[0], y[1], y[2], y[3]);
+        else if constexpr (VV == 2)
+          *reinterpret_cast<float2*>(vd) = make_float2(y[0], y[1]);
         else
           vd[0] = y[0];
         if (kSnap) {
