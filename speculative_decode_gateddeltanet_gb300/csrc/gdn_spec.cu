@@ -697,8 +697,8 @@ struct Stage {
   __host__ __device__ static int rows_floats(int R) { return R * 2 * DK + R * DVS + R * 4 + gram_floats(R); }
   // deferred mode: a previous call's carry rows, [Rp][DVS] u | [Rp][DK] k^ | [Rp4] exp(g)
   __host__ __device__ static int carry_floats(int Rp) { return Rp * DVS + Rp * DK + round4(Rp); }
-  __host__ __device__ static size_t bytes(int R, int Rp = 0) {
-    return sizeof(float) * ((size_t)DVS * DK + 2 * (size_t)(rows_floats(R) + carry_floats(Rp)));
+  __host__ __device__ static size_t bytes(int R, int Rp, int stages) {
+    return sizeof(float) * ((size_t)DVS * DK + stages * (size_t)(rows_floats(R) + carry_floats(Rp)));
   }
 };
 
@@ -749,8 +749,11 @@ __device__ __forceinline__ int lane_of_row(int m) {
   return off;
 }
 
-template <int DK, int MODE>
+// STAGES: buffers for an item's staged rows, 2 (the next item's rows land
+// while this one computes) or 1 (they land once this item is done with them).
+template <int DK, int MODE, int STAGES>
 __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(const Params p) {
+  constexpr bool one_stage = STAGES == 1;
   using Gm = Geo<DK>;
   constexpr int LPR = Gm::LPR, NC4 = Gm::NC4, RG = Gm::RG, M = Gm::M;
   constexpr int DVS = Gm::DVS, ROWS_W = Gm::ROWS_W;
@@ -883,21 +886,27 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   const bool writer = (lane & kDup) == 0;
   const size_t o_tstride = (size_t)p.H_v * p.d_v;
 
+  // With one rows stage an item's rows are copied once the item before it
+  // has finished reading the buffer.
+  int pend_it = -1, pend_rows = 0, pend_prev = 0;  // rows producer: copy deferred to the item's end
+
   for (int k = 0;; ++k) {
     const int it = blockIdx.x + k * gridDim.x;
     if (it >= n_items) break;
-    const int s = k & 1;
+    const int mi = k & 1;                                  // sMeta slot
+    const int s = one_stage ? 0 : mi;                      // rows stage
+    const uint32_t qpar = one_stage ? k & 1 : (k >> 1) & 1;  // phase of barQ[s] for this item
     // the arrive that completes each phase releases the producer's sMeta write
-    const bool late = !(mbar_wait(&barS, k & 1) && mbar_wait(&barQ[s], (k >> 1) & 1));
+    const bool late = !(mbar_wait(&barS, k & 1) && mbar_wait(&barQ[s], qpar));
     if (__syncthreads_or(late)) {
       if (tid == 0) flag(p.status, GDN_STATUS_TIMEOUT);
       mbar_wait(&barS, k & 1);  // bounded: let copies still in flight land before leaving
-      mbar_wait(&barQ[s], (k >> 1) & 1);
+      mbar_wait(&barQ[s], qpar);
       return;
     }
-    const int slot = sMeta[s][0], rows = sMeta[s][1];
-    const int prev = MODE == kDeferred ? sMeta[s][3] : 0;  // previous call's rows to commit first
-    const int a = MODE == kDeferred ? -1 : sMeta[s][2];    // commit row among this call's rows
+    const int slot = sMeta[mi][0], rows = sMeta[mi][1];
+    const int prev = MODE == kDeferred ? sMeta[mi][3] : 0;  // previous call's rows to commit first
+    const int a = MODE == kDeferred ? -1 : sMeta[mi][2];    // commit row among this call's rows
     const bool busy = rows > 0 || prev > 0;
 
     f2 S[M][NP];  // column pairs of the lane's 4-column chunks
@@ -923,10 +932,20 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         meta(it1, qn, m);  // loaded an item ago
         if (tid == 0) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) sMeta[s ^ 1][j] = m[j];
+          for (int j = 0; j < 4; ++j) sMeta[mi ^ 1][j] = m[j];
           issue_state(it1, m[0], m[1] + m[3]);
         }
-        if (tid == kRowsProducer) issue_rows(s ^ 1, it1, m[1], m[3]);
+        if (tid == kRowsProducer) {
+          if (!one_stage) {
+            issue_rows(s ^ 1, it1, m[1], m[3]);
+          } else if (!busy) {
+            issue_rows(0, it1, m[1], m[3]);  // this item does not use the buffer
+          } else {
+            pend_it = it1;
+            pend_rows = m[1];
+            pend_prev = m[3];
+          }
+        }
         if (it1 + gridDim.x < n_items) qn = load_req(it1 + gridDim.x);  // in flight while this item computes
       }
     }
@@ -1137,6 +1156,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       // ---- advance the state to the chunk's end when rows follow ----
       if (!last) combine(sQK + c0 * 2 * DK + DK, 2 * DK, nc, cdec, z, true, nullptr);
     }
+    if (one_stage) {
+      __syncthreads();  // every warp is done with the rows buffer: the next item's rows may land
+      if (tid == kRowsProducer && pend_it >= 0) {
+        fence_proxy_async();
+        issue_rows(0, pend_it, pend_rows, pend_prev);
+        pend_it = -1;
+      }
+    }
   }
   pdl_trigger();  // CTAs that had no item
 }
@@ -1197,32 +1224,47 @@ int prefer_max_shared(Kernel kernel) {
 template <int DK, int MODE>
 int launch_rows(const Params& p, cudaStream_t st) {
   using Gm = Geo<DK>;
-  const size_t smem = Stage<DK>::bytes(p.R, MODE == kDeferred ? p.Rp : 0);
+  const int Rp = MODE == kDeferred ? p.Rp : 0;
   struct Cache {
-    int dev = -1;
+    int dev = -1, R = -1, Rp = -1;
+    int stages = 2;
     size_t smem = 0;
-    int ctas = 0;  // resident CTAs on the device for this shared-memory size
+    int ctas = 0;  // resident CTAs on the device for this shape
   };
   static Cache cache;  // per instantiation
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
-  if (cache.dev != dev || cache.smem != smem) {
-    if (prefer_max_shared(rows_kernel<DK, MODE>) != GDN_OK) return GDN_ERR_LAUNCH;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(rows_kernel<DK, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  if (cache.dev != dev || cache.R != p.R || cache.Rp != Rp) {
+    // Double-buffered rows staging unless one buffer lets at least a quarter
+    // more CTAs be resident (long requests): measured, one more CTA per SM
+    // does not pay for the exposed copy of each item's rows, three more do.
+    const size_t smem2 = Stage<DK>::bytes(p.R, Rp, 2), smem1 = Stage<DK>::bytes(p.R, Rp, 1);
+    int per2 = 0, per1 = 0, sms = 0;
+    if (prefer_max_shared(rows_kernel<DK, MODE, 2>) != GDN_OK || prefer_max_shared(rows_kernel<DK, MODE, 1>) != GDN_OK)
+      return GDN_ERR_LAUNCH;
+    if (smem2 > 48 * 1024 &&
+        cudaFuncSetAttribute(rows_kernel<DK, MODE, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) !=
             cudaSuccess)
       return GDN_ERR_LAUNCH;
-    int per_sm = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rows_kernel<DK, MODE>, Gm::NT, smem) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per_sm < 1)
+    if (smem1 > 48 * 1024 &&
+        cudaFuncSetAttribute(rows_kernel<DK, MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) !=
+            cudaSuccess)
+      return GDN_ERR_LAUNCH;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, rows_kernel<DK, MODE, 2>, Gm::NT, smem2) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, rows_kernel<DK, MODE, 1>, Gm::NT, smem1) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per1 < 1)
       return GDN_ERR_LAUNCH;
     cache.dev = dev;
-    cache.smem = smem;
-    cache.ctas = per_sm * sms;
+    cache.R = p.R;
+    cache.Rp = Rp;
+    cache.stages = 4 * per1 >= 5 * per2 ? 1 : 2;
+    cache.smem = cache.stages == 2 ? smem2 : smem1;
+    cache.ctas = (cache.stages == 2 ? per2 : per1) * sms;
   }
   const long long items = (long long)p.B * p.H_v * p.slices;
   const int grid = (int)(items < cache.ctas ? items : cache.ctas);
-  return launch(rows_kernel<DK, MODE>, dim3(grid), dim3(Gm::NT), smem, st, p);
+  return cache.stages == 2 ? launch(rows_kernel<DK, MODE, 2>, dim3(grid), dim3(Gm::NT), cache.smem, st, p)
+                           : launch(rows_kernel<DK, MODE, 1>, dim3(grid), dim3(Gm::NT), cache.smem, st, p);
 }
 
 template <int MODE>
