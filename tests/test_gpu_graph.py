@@ -13,6 +13,12 @@ from speculative_decode_gateddeltanet_gb300.inputs import STACK, SWEEP, make_lay
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
 def _layers(name, **kw):
     return [make_layer(spec, seed) for spec, seed in workload_layers(name, **kw)]
 
@@ -94,3 +100,48 @@ def test_captured_step_sequence_matches_eager_steps():
         g.replay()
     torch.cuda.synchronize()
     _same([eager], [graphed])
+
+
+def test_captured_deferred_steps_match_eager():
+    """Two deferred steps of one layer: the first (nothing pending) writes its
+    carry, the second commits the first's accepted rows from that carry and
+    writes its own.  The pair captured as one graph and replayed equals the
+    same calls launched eagerly, bit for bit: o, both carries and the pools."""
+    from speculative_decode_gateddeltanet_gb300 import gdn
+    from speculative_decode_gateddeltanet_gb300.inputs import make_step
+
+    (first,) = _layers(STACK, layers=1)
+    second = make_step(first, first["spec"], 3100)
+    stream = torch.cuda.Stream()
+
+    def build():
+        d1 = gdn.DeviceLayer(first, "cuda")
+        d2 = gdn.DeviceLayer(second, "cuda")
+        d2.conv_state, d2.ssm_state = d1.conv_state, d1.ssm_state  # one slot pool
+        a1, a2 = d1.args(), d2.args()
+        d1.carry = torch.zeros(gdn.carry_bytes(a1) // 4, device="cuda")
+        d2.carry = torch.zeros(gdn.carry_bytes(a2) // 4, device="cuda")
+        a1.carry, a2.carry = d1.carry.data_ptr(), d2.carry.data_ptr()
+        prev = gdn.make_prev(x=d1.x, n_rows=d1.n_rows, accept_len=d1.accept_len, carry=d1.carry)
+        return d1, d2, a1, a2, prev
+
+    def step(a1, a2, prev):
+        gdn.gdn_verify_deferred(a1, None, stream)
+        gdn.gdn_verify_deferred(a2, prev, stream)
+
+    e1, e2, ea1, ea2, eprev = build()
+    with torch.cuda.stream(stream):
+        step(ea1, ea2, eprev)
+    torch.cuda.synchronize()
+    g1, g2, ga1, ga2, gprev = build()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step(ga1, ga2, gprev)
+    g.replay()
+    torch.cuda.synchronize()
+    for x, y in ((e1, g1), (e2, g2)):
+        assert torch.equal(bits(x.o), bits(y.o))
+        assert torch.equal(bits(x.carry), bits(y.carry))
+        assert int(x.status.item()) == int(y.status.item()) == 0
+    assert torch.equal(bits(e2.ssm_state), bits(g2.ssm_state))
+    assert torch.equal(bits(e2.conv_state), bits(g2.conv_state))
