@@ -3,29 +3,31 @@
 // Every call is two kernels on the caller's stream, chained by programmatic
 // dependent launch so the second one's state loads overlap the first:
 //
-// prep_kernel (one thread per channel): the width-4 causal conv + SiLU of
-//   every row over [committed window | verify rows], then the per-head L2
-//   norm of q and k.  Writes scale*q^, k^, v, the decay and write strength
-//   per row, and the rows' Gram tables k^.k^ and k^.(scale q^) into the
-//   caller's work buffer.  Each conv channel has exactly one reader in
-//   the call, so that thread also writes the channel's committed window
-//   (commit modes) or its per-row windows (snapshot mode).  The conv reads
-//   only the committed window and the verify rows, staging [history | verify
-//   inputs] per channel [FreeToken #844 "MTP drafts for Qwen3.5 family +
-//   Flash-Next", Design / Flash-Next target verify].
+// prep_kernel (one block per (request, q/k head) and per 256 VV value
+//   channels): the width-4 causal conv + SiLU of every row over [committed
+//   window | verify rows], then the per-head L2 norm of q and k.  Writes
+//   scale*q^, k^, v, the decay and write strength per row, and the rows'
+//   Gram tables k^.k^ and k^.(scale q^) into the caller's work buffer.  Each
+//   conv channel has exactly one reader in the call, so that thread also
+//   writes the channel's committed window (commit modes) or its per-row
+//   windows (snapshot mode).  The conv reads only the committed window and
+//   the verify rows, staging [history | verify inputs] per channel [FreeToken
+//   #844 "MTP drafts for Qwen3.5 family + Flash-Next", Design / Flash-Next
+//   target verify].  Before its dependency wait it only issues L2 hints for
+//   its own inputs.
 //
-// rows_kernel (one CTA per (request, value head, slice of DVS state rows)):
-//   loads its slice of the fp32 state S (DVS x d_k, d_k contiguous) with
-//   128-bit loads into registers before waiting on the prologue, stages the
-//   rows' q, k, v and tables from the work buffer with bulk async copies, and
-//   runs the gated delta rule S_t = alpha S + beta (v - alpha S k) k^T,
-//   o_t = scale S_t q with S resident in registers, in the chunked form
-//   described at the kernel (all dot products of a chunk of rows on the
-//   chunk's starting state, a scalar recurrence per state row, one state
-//   update).  Lanes own 4-float column chunks of 2 or 4 rows; a row's dot
-//   products are reduced over its 8 (d_k >= 32) or 4 (d_k = 16) lanes with a
-//   butterfly that leaves each lane holding one row's sums.  Arithmetic is
-//   fp32 with packed f32x2 FMA/MUL.
+// rows_kernel (persistent; item = (request, value head, slice of DVS state
+//   rows)): the slice of the fp32 state S (DVS x d_k, d_k contiguous) arrives
+//   by one bulk async copy, issued for the first item before the kernel waits
+//   on the prologue, and moves to registers; the item's q, k, v and tables
+//   are staged from the work buffer by bulk async copies.  It runs the gated
+//   delta rule S_t = alpha S + beta (v - alpha S k) k^T, o_t = scale S_t q
+//   with S resident in registers, in the chunked form described at the kernel
+//   (all dot products of a chunk of rows on the chunk's starting state, a
+//   scalar recurrence per state row, one state update).  Lanes own 4-float
+//   column chunks of 2 or 4 rows; a row's dot products are reduced over its
+//   8 (d_k >= 32) or 4 (d_k = 16) lanes with a butterfly that leaves each lane
+//   holding one row's sums.  Arithmetic is fp32 with packed f32x2 FMA/MUL.
 //
 // The arithmetic of a row does not depend on the mode, so a fused call, a
 // verify followed by a replay commit and a snapshot verify followed by a
@@ -35,10 +37,12 @@
 // "Speculative decoding: MTP and DFlash", Design]), verify with per-row
 // snapshots (the widened verify state of [LightLLM #1330 "Qwen3.5 /
 // Qwen3.5-MoE MTP speculative decoding", Summary]), replay commit (rows
-// 0..a rerun from the slot, then written once), and fused verify + commit
-// (the slot is written at row a from the registers: one read and one write
-// of the state per request, the verify-and-commit kernel mode of [lmdeploy
-// #5006 "speculative decoding for TurboMind", Verification path]).
+// 0..a rerun from the slot, then written once), fused verify + commit (the
+// slot is written at row a from the registers: one read and one write of the
+// state per request, the verify-and-commit kernel mode of [lmdeploy #5006
+// "speculative decoding for TurboMind", Verification path]), and deferred
+// (the previous call's accepted rows committed from its carry, then this
+// call's rows verified; the accept-count carry of [LightLLM #1330, Summary]).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -680,7 +684,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
 // slice has one shared-memory buffer: as soon as an item's slice is in
 // registers, the next item's slice (one bulk copy) is requested, so it is in
 // flight while the item computes.  The item's q/k rows, v rows, per-row
-// scalars and Gram tables are small and double-buffered.
+// scalars and Gram tables are small and double-buffered, or single-buffered
+// when that lets a quarter more CTAs be resident (long requests).  In
+// deferred mode an item first commits the previous call's rows from its
+// carry (one rank-(a+1) update of the registers, stored to the slot).
 //
 // The rows of an item run in chunks of up to CH rows.  With C_t the product of
 // the decays of the chunk's rows up to t and z_s^(t) = (C_t / C_s) u_s, the
