@@ -110,6 +110,9 @@ CASES = [
      spec_of(64, 3, k_choices=(1, 3), inactive_frac=0.1)),
     ("d_k64", spec_of(4, 2, shape=dict(H_qk=4, H_v=8, d_k=64, d_v=64)),
      spec_of(4, 3, shape=dict(H_qk=4, H_v=8, d_k=64, d_v=64))),
+    ("d_k32-16-rows-both", spec_of(4, 15, shape=dict(H_qk=2, H_v=4, d_k=32, d_v=64)),
+     spec_of(4, 15, shape=dict(H_qk=2, H_v=4, d_k=32, d_v=64))),
+    ("d_k16-f32-k7-then-k0", spec_of(3, 7, "f32", TINY_SHAPE), spec_of(3, 0, "f32", TINY_SHAPE)),
 ]
 
 
