@@ -286,3 +286,29 @@ def test_raw_gating_matches_oracle(name, batch, mode):
     dev = run_gpu(layer, mode, raw_gating=True)
     check_against_oracle(layer, dev, ref, commit=True)
     assert int(dev.status.item()) == 0
+
+
+DEGENERATE = {
+    "no_write": (0.0, 0.0),        # g = 0, beta = 0: the state is only read (S unchanged, o = scale S0 q)
+    "exact_write": (0.0, 1.0),     # g = 0, beta = 1: each row overwrites S k = v
+    "full_decay": (-200.0, 1.0),   # exp(g) = 0 in fp32: each row leaves S = v k^T
+}
+
+
+@pytest.mark.parametrize("case", sorted(DEGENERATE))
+@pytest.mark.parametrize("mode", MODES)
+def test_degenerate_gating(case, mode):
+    """The recurrence's special cases through the whole CUDA path: no write,
+    exact write and full decay (decay products underflowing to zero inside
+    a chunk), against the oracle; with no write the committed state equals
+    the input state bit for bit."""
+    g_val, b_val = DEGENERATE[case]
+    spec = LayerSpec("degenerate", B=4, k=3, H_qk=16, H_v=32, d_k=128, d_v=128, pool="perm")
+    layer = make_layer(spec, 77)
+    layer["g"] = torch.full_like(layer["g"], g_val)
+    layer["beta"] = torch.full_like(layer["beta"], b_val)
+    dev = run_gpu(layer, mode)
+    check_against_oracle(layer, dev, oracle.verify_commit(layer), commit=True)
+    assert int(dev.status.item()) == 0
+    if case == "no_write":
+        assert torch.equal(bits(dev.ssm_state), bits(layer["ssm_state"]))
