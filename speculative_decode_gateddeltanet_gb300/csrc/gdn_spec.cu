@@ -48,6 +48,7 @@
 #include <stdint.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "gdnspec.h"
 
@@ -1226,52 +1227,72 @@ int prefer_max_shared(Kernel kernel) {
              : GDN_ERR_LAUNCH;
 }
 
+// Once per kernel instantiation and device (bit dev of done): the max-shared
+// carveout and a dynamic shared-memory cap large enough for every shape, so
+// no later call lowers what a concurrent launch relies on.  Racing first
+// calls set the same values.
+template <typename Kernel>
+int setup_kernel(Kernel kernel, size_t max_smem, std::atomic<unsigned long long>& done, int dev) {
+  if (dev < 0 || dev >= 64) return GDN_ERR_UNSUPPORTED;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return GDN_OK;
+  if (prefer_max_shared(kernel) != GDN_OK) return GDN_ERR_LAUNCH;
+  if (max_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return GDN_OK;
+}
+
 // Persistent grid of the rows kernel: as many CTAs as fit at once (at most one
 // per item).
 template <int DK, int MODE>
 int launch_rows(const Params& p, cudaStream_t st) {
   using Gm = Geo<DK>;
   const int Rp = MODE == kDeferred ? p.Rp : 0;
-  struct Cache {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
+  static std::atomic<unsigned long long> set1{0}, set2{0};
+  const int max_rp = MODE == kDeferred ? kMaxR : 0;
+  int rc = setup_kernel(rows_kernel<DK, MODE, 1>, Stage<DK>::bytes(kMaxR, max_rp, 1), set1, dev);
+  if (rc == GDN_OK) rc = setup_kernel(rows_kernel<DK, MODE, 2>, Stage<DK>::bytes(kMaxR, max_rp, 2), set2, dev);
+  if (rc != GDN_OK) return rc;
+  // Double-buffered rows staging unless one buffer lets at least a quarter
+  // more CTAs be resident (long requests): measured, one more CTA per SM
+  // does not pay for the exposed copy of each item's rows, three more do.
+  struct Choice {
     int dev = -1, R = -1, Rp = -1;
     int stages = 2;
     size_t smem = 0;
     int ctas = 0;  // resident CTAs on the device for this shape
   };
-  static Cache cache;  // per instantiation
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
-  if (cache.dev != dev || cache.R != p.R || cache.Rp != Rp) {
-    // Double-buffered rows staging unless one buffer lets at least a quarter
-    // more CTAs be resident (long requests): measured, one more CTA per SM
-    // does not pay for the exposed copy of each item's rows, three more do.
-    const size_t smem2 = Stage<DK>::bytes(p.R, Rp, 2), smem1 = Stage<DK>::bytes(p.R, Rp, 1);
-    int per2 = 0, per1 = 0, sms = 0;
-    if (prefer_max_shared(rows_kernel<DK, MODE, 2>) != GDN_OK || prefer_max_shared(rows_kernel<DK, MODE, 1>) != GDN_OK)
-      return GDN_ERR_LAUNCH;
-    if (smem2 > 48 * 1024 &&
-        cudaFuncSetAttribute(rows_kernel<DK, MODE, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) !=
-            cudaSuccess)
-      return GDN_ERR_LAUNCH;
-    if (smem1 > 48 * 1024 &&
-        cudaFuncSetAttribute(rows_kernel<DK, MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) !=
-            cudaSuccess)
-      return GDN_ERR_LAUNCH;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, rows_kernel<DK, MODE, 2>, Gm::NT, smem2) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, rows_kernel<DK, MODE, 1>, Gm::NT, smem1) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per1 < 1)
-      return GDN_ERR_LAUNCH;
-    cache.dev = dev;
-    cache.R = p.R;
-    cache.Rp = Rp;
-    cache.stages = 4 * per1 >= 5 * per2 ? 1 : 2;
-    cache.smem = cache.stages == 2 ? smem2 : smem1;
-    cache.ctas = (cache.stages == 2 ? per2 : per1) * sms;
+  static std::mutex mu;
+  static Choice last;  // per instantiation: the last shape's choice
+  Choice c;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (last.dev != dev || last.R != p.R || last.Rp != Rp) {
+      const size_t smem2 = Stage<DK>::bytes(p.R, Rp, 2), smem1 = Stage<DK>::bytes(p.R, Rp, 1);
+      int per2 = 0, per1 = 0, sms = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, rows_kernel<DK, MODE, 2>, Gm::NT, smem2) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, rows_kernel<DK, MODE, 1>, Gm::NT, smem1) !=
+              cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per1 < 1)
+        return GDN_ERR_LAUNCH;
+      last.dev = dev;
+      last.R = p.R;
+      last.Rp = Rp;
+      last.stages = 4 * per1 >= 5 * per2 ? 1 : 2;
+      last.smem = last.stages == 2 ? smem2 : smem1;
+      last.ctas = (last.stages == 2 ? per2 : per1) * sms;
+    }
+    c = last;
   }
   const long long items = (long long)p.B * p.H_v * p.slices;
-  const int grid = (int)(items < cache.ctas ? items : cache.ctas);
-  return cache.stages == 2 ? launch(rows_kernel<DK, MODE, 2>, dim3(grid), dim3(Gm::NT), cache.smem, st, p)
-                           : launch(rows_kernel<DK, MODE, 1>, dim3(grid), dim3(Gm::NT), cache.smem, st, p);
+  const int grid = (int)(items < c.ctas ? items : c.ctas);
+  return c.stages == 2 ? launch(rows_kernel<DK, MODE, 2>, dim3(grid), dim3(Gm::NT), c.smem, st, p)
+                       : launch(rows_kernel<DK, MODE, 1>, dim3(grid), dim3(Gm::NT), c.smem, st, p);
 }
 
 template <int MODE>
@@ -1293,13 +1314,11 @@ int launch_prep_r(const Params& p, cudaStream_t st) {
   constexpr int VV = vec_v<RMAX>();
   const int v_blocks = (p.H_v * p.d_v + kPrepThreads * VV - 1) / (kPrepThreads * VV);
   const dim3 grid(p.H_qk + v_blocks, p.B), block(kPrepThreads);
-  static int set_on = -1;  // device on which this instantiation's carveout was last set
+  static std::atomic<unsigned long long> set{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
-  if (set_on != dev) {
-    if (prefer_max_shared(prep_kernel<T, MODE, RMAX>) != GDN_OK) return GDN_ERR_LAUNCH;
-    set_on = dev;
-  }
+  const int rc = setup_kernel(prep_kernel<T, MODE, RMAX>, 0, set, dev);
+  if (rc != GDN_OK) return rc;
   return launch(prep_kernel<T, MODE, RMAX>, grid, block, 0, st, p);
 }
 
