@@ -47,6 +47,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -1589,7 +1590,6 @@ GDN_API const char* gdn_strerror(int code) {
 // device address (on the host it names a stand-in object); its device address
 // is looked up once per device with cudaGetSymbolAddress while that device is
 // current, cached, and passed to the kernels like any work buffer.
-#include <atomic>
 
 namespace gdnspec {
 static __device__ __align__(256) unsigned char g_static_work[GDN_STATIC_WORK_BYTES];
