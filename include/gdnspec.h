@@ -262,8 +262,9 @@ GDN_API size_t gdn_carry_bytes(const gdn_args* args);
  *   status      [1]        int32, may be NULL; GDN_STATUS_BAD_NROWS for n_rows outside [0, R]
  *
  * Two kernels on `stream` (a cluster of 8 CTAs per verify row, then one
- * thread per request), chained by programmatic dependent launch; allocates
- * nothing and does not synchronise.  Returns GDN_ERR_INVALID_ARG,
+ * thread per request), chained by programmatic dependent launch; the first
+ * waits for the kernel before it on the stream.  Allocates nothing and does
+ * not synchronise.  Returns GDN_ERR_INVALID_ARG,
  * GDN_ERR_UNSUPPORTED (V % 8 != 0, B or R > 65535, dtype),
  * GDN_ERR_MISALIGNED or GDN_ERR_LAUNCH before launching anything. */
 typedef struct gdn_accept_args {

@@ -67,6 +67,7 @@ __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) argmax_kernel(const Params p) {
+  pdl_wait();     // the logits of the kernel before are complete and visible
   pdl_trigger();  // the acceptance kernel may launch; it waits for this grid before reading
   __shared__ float sv[kThreads / 32];
   __shared__ int si[kThreads / 32];
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const Params p) {
                                                     ((size_t)b * p.R + t) * p.V);
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = 5;  // a 151936-token bf16 row slice in one batch of loads per thread
   for (int c = c0 + threadIdx.x; c < c1; c += kUnroll * kThreads) {
     uint4 w[kUnroll];
 #pragma unroll
