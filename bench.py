@@ -257,7 +257,9 @@ def run_cuda(args, rank, ws, local):
                 gdn.gdn_verify(a, m, sp)
                 gdn.gdn_commit(a, m, sp)
 
-    launches_per_step = len(cargs) * (1 if args.mode in ("fused", "deferred") else 2)
+    calls_per_step = len(cargs) * (1 if args.mode in ("fused", "deferred") else 2)
+    # kernels per layer: prologue + rows kernel per call; a snapshot commit is one kernel
+    kernels_per_layer = {"fused": 2, "deferred": 2, "replay": 4, "snapshot": 3}[args.mode]
     # --graph: the step's launches captured once into a CUDA graph and replayed
     graph = None
 
@@ -333,7 +335,7 @@ def run_cuda(args, rank, ws, local):
 
     peak, peak_kind = hbm_peak()
     per_launch_bytes = bytes_per_step / len(cargs)
-    launch_s = ms_step / 1e3 / launches_per_step
+    launch_s = ms_step / 1e3 / calls_per_step
     achieved = (per_launch_bytes / launch_s / 1e9 if args.mode in ("fused", "deferred")
                 else bytes_per_step / (ms_step / 1e3) / 1e9)
     out = {
@@ -355,7 +357,7 @@ def run_cuda(args, rank, ws, local):
                      "algorithmic_bytes_per_launch": round(per_launch_bytes)},
         "e2e": {"value": round(rows_per_step * ws / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": kernels_per_layer * len(cargs) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
