@@ -10,8 +10,9 @@ __all__ = ["gdn", "inputs", "build"]
 
 
 def __getattr__(name):
-    if name in ("gdn_verify", "gdn_commit", "gdn_verify_commit", "GdnArgs", "GdnError", "make_args",
-                "DeviceLayer", "REPLAY", "SNAPSHOT", "strerror"):
+    if name in ("gdn_verify", "gdn_commit", "gdn_verify_commit", "gdn_verify_commit_static",
+                "gdn_verify_deferred", "greedy_accept", "GdnArgs", "GdnPrevRows", "GdnError", "make_args",
+                "make_prev", "work_bytes", "carry_bytes", "DeviceLayer", "REPLAY", "SNAPSHOT", "strerror"):
         from . import gdn
 
         return getattr(gdn, name)

@@ -181,7 +181,8 @@ class DeviceLayer:
 
     Built from a dict of CPU tensors (the layout ``inputs.make_layer`` uses).
     ``o`` is filled with NaN so rows a call must not write stay visibly
-    untouched; ``status`` starts at zero; ``work`` is sized by the library."""
+    untouched; ``status`` starts at zero; ``work`` is sized by the library.
+    ``carry`` (None until set) is passed as the call's carry for deferred calls."""
 
     KEYS = ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows", "accept_len")
 
@@ -203,6 +204,7 @@ class DeviceLayer:
             self.scratch_S = torch.empty((s.B, s.R, s.H_v, s.d_v, s.d_k), device=device)
             self.scratch_cs = torch.empty((s.B, s.R, s.C, s.W - 1), dtype=self.x.dtype, device=device)
         self.scale, self.l2_eps = scale, l2_eps
+        self.carry = None
         self.work = None
         self.work = torch.empty(work_bytes(self.args()) // 4, dtype=torch.float32, device=device)
 
@@ -212,7 +214,7 @@ class DeviceLayer:
                          slot_ids=self.slot_ids, n_rows=self.n_rows, accept_len=self.accept_len,
                          o=self.o, scratch_S=self.scratch_S, scratch_cs=self.scratch_cs,
                          work=self.work, status=self.status, H_qk=self.spec.H_qk,
-                         scale=self.scale, l2_eps=self.l2_eps, A_log=self.A_log)
+                         scale=self.scale, l2_eps=self.l2_eps, A_log=self.A_log, carry=self.carry)
 
 
 def greedy_accept(logits, drafts, n_rows, target, accept_len, status=None, stream=None) -> GdnAcceptArgs:
