@@ -56,7 +56,12 @@
  * use distinct slots; two calls that touch the same slots or the same work
  * buffer must not run concurrently.  Each call is two kernel launches (a
  * prologue and the rows) chained with programmatic dependent launch; the
- * prologue waits for whatever ran before it on the stream.  In replay mode the verify and the commit must see
+ * prologue waits for whatever ran before it on the stream.  The rows kernel
+ * lets the next kernel on the stream launch early, as each of its CTAs starts
+ * its last item: a following kernel launched with programmatic stream
+ * serialization must wait (griddepcontrol.wait, cudaGridDependencySynchronize)
+ * before it reads this call's outputs, as any such dependent must; kernels
+ * launched without that attribute start after this call has finished.  In replay mode the verify and the commit must see
  * the same x, g, beta, conv_w and slot contents.
  *
  * Errors.  Host return codes: GDN_OK, or GDN_ERR_* for arguments the host
