@@ -61,8 +61,9 @@
  * its last item: a following kernel launched with programmatic stream
  * serialization must wait (griddepcontrol.wait, cudaGridDependencySynchronize)
  * before it reads this call's outputs, as any such dependent must; kernels
- * launched without that attribute start after this call has finished.  In replay mode the verify and the commit must see
- * the same x, g, beta, conv_w and slot contents.
+ * launched without that attribute start after this call has finished.  In
+ * replay mode the verify and the commit must see the same x, g, beta, conv_w
+ * and slot contents.
  *
  * Errors.  Host return codes: GDN_OK, or GDN_ERR_* for arguments the host
  * can check (null pointers, shapes, alignment; nothing is launched) and for a
