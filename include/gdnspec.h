@@ -6,8 +6,8 @@
  * The operation.  A verify step scores, per request, the k+1 rows
  * [pending, d1..dk] in one pass [FreeToken #844 "MTP drafts for Qwen3.5
  * family + Flash-Next", Design; FreeToken #828 "Speculative decoding: MTP and
- * DFlash", Design: "a uniform extend of k+1 rows per request"].  Each row runs
- * one GDN decode step:
+ * DFlash", Design: every request extends by the same k+1 rows].  Each row
+ * runs one GDN decode step:
  *   window_t[c] = last W entries of [conv_state[c][0..W-2], x_0[c] .. x_t[c]]
  *   y_t[c]      = SiLU(sum_j conv_w[c][j] * window_t[c][j])   (tap W-1 = newest)
  *   q, k        = per q/k head  y / sqrt(sum y^2 + l2_eps),  v = v block of y
@@ -16,7 +16,7 @@
  *     o_t = scale * S_t q
  * The GDN state is only read during the verify; the commit then makes each
  * request's slot hold the state after its accepted rows [FreeToken #828,
- * Design], with the conv window "as it stands after the accepted rows"
+ * Design], with the conv window left where the accepted rows put it
  * [FreeToken #844, Flash-Next target verify].  accept_len = a counts accepted
  * drafts; the commit covers rows 0..a (a+1 tokens, the pages' "accept
  * length", FreeToken #844, End-to-end).  The verify may also snapshot every
@@ -113,7 +113,21 @@ enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
  *   g = -exp(A_log[h]) * softplus(a),   beta = sigmoid(b)
  * (the standard gating of a Qwen3.5-style GDN layer; the pages feed the
  * recurrence these per-head scalars without printing how they are formed). */
-enum { GDN_FLAG_RAW_GATING = 1 };
+/* GDN_FLAG_STATE_STABLE - a promise by the caller that no kernel that may
+ * still be running on `stream` when this call is made writes this call's
+ * ssm_state or conv_state slots, slot_ids or n_rows (for gdn_verify_deferred:
+ * nor prev->n_rows).  With it the call starts fetching its state slices while
+ * the kernels ahead of it on the stream are still draining, instead of after
+ * they have finished: in a model, while the projection that writes x, g and
+ * beta still runs; in a stack of layers, while the previous layer's call
+ * finishes.  Everything else the call reads (x, g, beta, conv_w, A_log,
+ * accept_len, the previous call's carry) is still read only after the kernels
+ * ahead of it have finished, so accept_len may come from gdn_greedy_accept
+ * launched just before.  Without the promise (flag clear) nothing is read
+ * before those kernels finish.  The results are the same bits either way.
+ * Two calls in a row on the same slots (the same layer's consecutive decode
+ * steps with nothing in between) must not set it on the second call. */
+enum { GDN_FLAG_RAW_GATING = 1, GDN_FLAG_STATE_STABLE = 2 };
 enum { GDN_REPLAY = 0, GDN_SNAPSHOT = 1 };
 
 typedef struct gdn_args {
@@ -128,7 +142,7 @@ typedef struct gdn_args {
   int32_t in_dtype;   /* GDN_DTYPE_* of x, conv_w, conv_state, scratch_cs      */
   float scale;        /* o = scale * S q (usually d_k^-1/2), finite            */
   float l2_eps;       /* >= 0, added to sum y^2 before the square root         */
-  int32_t flags;      /* 0 or GDN_FLAG_RAW_GATING                              */
+  int32_t flags;      /* 0, or GDN_FLAG_RAW_GATING | GDN_FLAG_STATE_STABLE     */
   const void* x;      /* 16-byte aligned: x, conv_w, conv_state, ssm_state, o,  */
   const float* g;     /* scratch_S, scratch_cs; 4-byte: g, beta, int32 arrays   */
   const float* beta;
@@ -222,6 +236,10 @@ GDN_API const char* gdn_strerror(int code);
  *   n_rows      [B]           int32     its valid rows; 0 = nothing pending for request b
  *   accept_len  [B]           int32     its accepted drafts, 0..n_rows-1 when n_rows > 0
  *   carry                               the previous deferred call's cur->carry, unchanged
+ * prev->carry and cur->carry must not overlap, nor prev->x and cur->x: a step
+ * reads the previous step's carry and rows while it writes its own, so both
+ * are double-buffered across steps (overlapping ranges return
+ * GDN_ERR_INVALID_ARG before anything is launched).
  * prev may be NULL (nothing pending for any request: the first step).  The
  * result equals gdn_commit (replay) of the previous step followed by
  * gdn_verify of the current one.  prev->R <= 16, like every R.  Only the
@@ -254,7 +272,8 @@ GDN_API size_t gdn_carry_bytes(const gdn_args* args);
  *
  * For every request b with 0 < n_rows[b] <= R and every verify row
  * t < n_rows[b]:  target[b][t] = the index of the largest logits[b][t][:]
- * (the lowest index among equal largest values; NaN entries never win).
+ * (the lowest index among equal largest values; NaN entries never win, and a
+ * row whose entries are all NaN gives 0).
  * Then accept_len[b] = the largest a <= n_rows[b]-1 with drafts[b][i] ==
  * target[b][i] for all i < a: draft i+1 is the token at verify row i+1 and
  * is kept when the target chose it at row i.  target[b][a] is the target's
@@ -269,8 +288,10 @@ GDN_API size_t gdn_carry_bytes(const gdn_args* args);
  *
  * Two kernels on `stream` (a cluster of 8 CTAs per verify row, then one
  * thread per request), chained by programmatic dependent launch; the first
- * waits for the kernel before it on the stream.  Allocates nothing and does
- * not synchronise.  Returns GDN_ERR_INVALID_ARG,
+ * waits for the kernel before it on the stream, and the second lets the next
+ * kernel launch early (a following kernel launched with programmatic stream
+ * serialization must wait before it reads target or accept_len, as the
+ * calls of this library do).  Allocates nothing and does not synchronise.  Returns GDN_ERR_INVALID_ARG,
  * GDN_ERR_UNSUPPORTED (V % 8 != 0, B or R > 65535, dtype),
  * GDN_ERR_MISALIGNED or GDN_ERR_LAUNCH before launching anything. */
 typedef struct gdn_accept_args {

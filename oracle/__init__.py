@@ -143,6 +143,56 @@ def verify_commit(layer: dict, *, commit: bool = True, snapshot: bool = False,
     return out
 
 
+def verify_commit_threads(layer: dict, threads: int, *, scale: float | None = None,
+                          l2_eps: float = DEFAULT_EPS) -> dict:
+    """``verify_commit`` (fused verify + commit) with the requests spread over
+    ``threads`` host threads: thread i runs the same C routine on requests
+    b = i, i + threads, ... with the others masked inactive.  Requests touch
+    disjoint slots and output rows, and the routine keeps no state between
+    calls, so the threads share the arrays and the result equals
+    ``verify_commit``'s exactly.  ctypes releases the interpreter lock during
+    each C call, so the threads run in parallel.  ``seconds`` is the wall time
+    of the parallel region (marshalling excluded, as in ``verify_commit``)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    spec = layer["spec"]
+    B, R, C, W = spec.B, spec.R, spec.C, spec.W
+    dims = _Dims(B, R, spec.H_qk, spec.H_v, spec.d_k, spec.d_v, W, spec.pool_slots,
+                 spec.d_k ** -0.5 if scale is None else scale, l2_eps)
+    x, g, beta = _f64(layer["x"]), _f64(layer["g"]), _f64(layer["beta"])
+    conv_w = _f64(layer["conv_w"])
+    conv_state = _f64(layer["conv_state"]).copy()
+    ssm_state = _f64(layer["ssm_state"]).copy()
+    slots = _i32(layer["slot_ids"])
+    n_all = _i32(layer["n_rows"])
+    acc = _i32(layer["accept_len"])
+    o = np.full((B, R, spec.H_v, spec.d_v), np.nan)
+    threads = max(1, min(int(threads), B))
+    masks = []
+    for i in range(threads):
+        n = np.zeros_like(n_all)
+        n[i::threads] = n_all[i::threads]
+        masks.append(n)
+    lib = _load()
+    dp, ip = ctypes.c_double, ctypes.c_int
+
+    def run(n):
+        return lib.oracle_gdn_verify_commit(
+            ctypes.byref(dims), _ptr(x, dp), _ptr(g, dp), _ptr(beta, dp), _ptr(conv_w, dp),
+            _ptr(conv_state, dp), _ptr(ssm_state, dp), _ptr(slots, ip), _ptr(n, ip),
+            _ptr(acc, ip), _ptr(o, dp), None, None, 0)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        t0 = time.perf_counter()
+        statuses = list(ex.map(run, masks))
+        seconds = time.perf_counter() - t0
+    status = 0
+    for st in statuses:
+        status |= int(st)
+    return {"o": o, "ssm_state": ssm_state, "conv_state": conv_state, "status": status,
+            "seconds": seconds, "threads": threads}
+
+
 def verify_deferred(cur: dict, prev: dict | None = None, *, requests=None, scale: float | None = None,
                     l2_eps: float = DEFAULT_EPS, raw_gating: bool = False) -> dict:
     """Deferred commit on the CPU, by its definition: the previous step's rows

@@ -15,8 +15,8 @@
  *    Design].
  *   The GDN state is only read during the verify; the commit leaves each
  *   request's slot as a+1 decode steps would leave it, where a is the number
- *   of accepted drafts, restoring the conv window "as it stands after the
- *   accepted rows" [FreeToken #828, Design; FreeToken #844 "MTP drafts for
+ *   of accepted drafts, with the conv window moved on over exactly the
+ *   accepted rows [FreeToken #828, Design; FreeToken #844 "MTP drafts for
  *   Qwen3.5 family + Flash-Next", Design / Flash-Next target verify].
  *   The accept length those pages print counts committed tokens, a+1, at most
  *   k+1 [FreeToken #844, End-to-end].

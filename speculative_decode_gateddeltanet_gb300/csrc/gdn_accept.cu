@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const Params p) {
       asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(i2) : "r"(peer_addr(&ci, r)) : "memory");
       better(v, i, v2, i2);
     }
-    p.target[(size_t)b * p.R + t] = i;
+    // no entry ever won: every logit of the row is NaN, and the row's token is 0
+    p.target[(size_t)b * p.R + t] = i == 0x7fffffff ? 0 : i;
   }
   cluster_sync();  // no CTA leaves while rank 0 reads its shared memory
 }
@@ -149,7 +150,8 @@ __global__ void __launch_bounds__(kThreads) argmax_kernel(const Params p) {
 // target chose at row i.  Inactive requests (n_rows 0) get 0; a bad n_rows
 // gets 0 and a status bit.
 __global__ void __launch_bounds__(256) accept_kernel(const Params p) {
-  pdl_wait();  // the target tokens are complete and visible
+  pdl_wait();     // the target tokens are complete and visible
+  pdl_trigger();  // the next kernel may launch; it waits for this grid before reading accept_len
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= p.B) return;
   const int n = p.n_rows[b];

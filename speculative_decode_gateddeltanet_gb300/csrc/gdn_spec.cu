@@ -95,6 +95,10 @@ struct Params {
   int* status;
   const float* A_log;  // GDN_FLAG_RAW_GATING: g and beta hold the raw projections a and b
   int raw_gating;
+  // GDN_FLAG_STATE_STABLE: nothing still running on the stream writes this call's
+  // slots, slot_ids or n_rows, so the rows kernel may fetch state slices before
+  // the kernels ahead of it have finished
+  int early;
   // Deferred commit.  Request b's block of conv rows is the previous call's
   // rows 0..acc_prev[b] (when n_prev[b] > 0; they only advance the window)
   // then its current rows.  The state rows run the current rows only, after
@@ -228,11 +232,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-// Waits for phase `parity` of the barrier; gives up after a bounded number of
-// polls (each poll may itself suspend briefly) and returns false.
+// How long a staging wait may last before the kernel gives up on it (ns of
+// %globaltimer).  A copy lands in microseconds; the limit only has to catch a
+// barrier whose bytes will never all arrive.
+#ifndef GDN_WAIT_LIMIT_NS
+#define GDN_WAIT_LIMIT_NS 500000000ull
+#endif
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for phase `parity` of the barrier; gives up and returns false once
+// GDN_WAIT_LIMIT_NS have passed (the clock is read every 256 polls; 2^24 polls
+// end the wait whatever the clock says).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  constexpr int kMaxPolls = 1 << 22;
-  for (int i = 0; i < kMaxPolls; ++i) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 1; i < (1u << 24); ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -240,9 +256,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     if (done) return true;
+    if ((i & 255) == 0) {
+      const uint64_t now = global_ns();
+      if (t0 == 0)
+        t0 = now;
+      else if (now - t0 > GDN_WAIT_LIMIT_NS)
+        return false;
+    }
   }
   return false;
 }
+
+#ifdef GDN_TEST_HOOKS
+// Test builds only: the rows-kernel item whose state copy the producer
+// declares on its barrier but never issues, so that item's wait runs out with
+// no copy in flight (-1: none).  Set by gdn_test_drop_state_copy.
+__device__ int g_test_drop_item = -1;
+#endif
 
 // Validity of a request as every kernel reads it, from its n_rows n, slot and
 // accept length a.  Returns the number of rows to run (0 = nothing to do for
@@ -364,8 +394,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
         prefetch_l2(src, (uint32_t)bytes);
     }
   }
-  pdl_wait();     // whatever ran before on the stream is complete and visible
-  pdl_trigger();  // the rows kernel may start loading its state
+  // The rows kernel may start loading its state once every block has passed
+  // here: with the caller's promise that nothing still running writes the
+  // state, before this block's wait; else after it.
+  if (p.early) pdl_trigger();
+  pdl_wait();  // whatever ran before on the stream is complete and visible
+  if (!p.early) pdl_trigger();
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
 
   const int b = blockIdx.y;
@@ -778,6 +812,14 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   const int n_items = p.B * p.H_v * p.slices;
   const int R = p.R;
   const int Rp = MODE == kDeferred ? p.Rp : 0;
+  // The CTA's k-th item (-1 past its last).  Full rounds k < Q give CTA j item
+  // k G + j.  The partial last round's E < G items go to the CTAs j with
+  // floor((j+1) E / G) > floor(j E / G): an even share of every run of
+  // consecutive CTAs.  CTAs that become resident together tend to share SMs,
+  // so handing the partial round to the first E CTAs loads some SMs with two
+  // items per CTA and leaves others with one; spread, each SM gets its share.
+  // The CTA's item after item `it` (-1: none): CTA j runs items j, j + G, j + 2G, ...
+  auto next_item = [&](int it) -> int { return it + (int)gridDim.x < n_items ? it + (int)gridDim.x : -1; };
   const int rfl = Stage<DK>::rows_floats(R) + Stage<DK>::carry_floats(Rp);
   extern __shared__ __align__(16) float smem[];
   float* const stS = smem;  // [DVS][DK] state slice of the next item
@@ -834,6 +876,9 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     const int b = it / (p.H_v * p.slices);
     const int hs = it - b * p.H_v * p.slices;  // h * slices + sl
     mbar_expect_tx(&barS, kSBytes);
+#ifdef GDN_TEST_HOOKS
+    if (it == g_test_drop_item) return;  // declared, never issued: the item's wait runs out
+#endif
     bulk_load(stS, p.S + ((size_t)slot * p.H_v * p.slices + hs) * DVS * DK, kSBytes, &barS);
   };
   // rows: current rows to stage; prev: previous rows whose carry is staged (deferred mode)
@@ -871,21 +916,39 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   constexpr int kRowsProducer = Gm::NT > 32 ? 32 : 0;
   const bool producer = tid == 0 || tid == kRowsProducer;
   Req qn{0, 0, -1, 0};  // producer: request data of the item after the current one
-  if (tid == kRowsProducer && blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);
+  const int it0 = (int)blockIdx.x < n_items ? (int)blockIdx.x : -1;
+  const int it1st = it0 >= 0 ? next_item(it0) : -1;
+  if (!p.early && tid == kRowsProducer && it1st >= 0) qn = load_req(it1st);
   if (tid == 0) {
     mbar_init(&barS, 1);
     mbar_init(&barQ[0], 1);
     mbar_init(&barQ[1], 1);
-    if (blockIdx.x < n_items) {
-      const Req q0 = load_req(blockIdx.x);
-      if (blockIdx.x + gridDim.x < n_items) qn = load_req(blockIdx.x + gridDim.x);  // both in flight
-      meta(blockIdx.x, q0, sMeta[0]);
-      issue_state(blockIdx.x, sMeta[0][0], sMeta[0][1] + sMeta[0][3]);  // before the prologue has finished
+    if (it0 >= 0) {
+      if (p.early) {
+        // Only the slot and the row count are read before the wait (the
+        // caller promised nothing in flight writes them or the state); the
+        // slice is fetched whenever the request could need it, and what the
+        // item does with it is decided after the wait.
+        const int b = it0 / (p.H_v * p.slices);
+        const int slot = p.slot_ids[b], n = p.n_rows[b];
+        const bool need = slot >= 0 && slot < p.P && n >= 0 && n <= p.R && (n > 0 || MODE == kDeferred);
+        issue_state(it0, slot, need ? 1 : 0);
+      } else {
+        const Req q0 = load_req(it0);
+        if (it1st >= 0) qn = load_req(it1st);  // both in flight
+        meta(it0, q0, sMeta[0]);
+        issue_state(it0, sMeta[0][0], sMeta[0][1] + sMeta[0][3]);  // before the prologue has finished
+      }
     }
   }
   __syncthreads();  // the barriers are initialised before anyone waits on them
   pdl_wait();       // the prologue's q, k, v and tables are complete and visible
-  if (tid == kRowsProducer && blockIdx.x < n_items) issue_rows(0, blockIdx.x, sMeta[0][1], sMeta[0][3]);
+  if (p.early) {    // the rest of the request data, now that the kernels before have finished
+    if (tid == 0 && it0 >= 0) meta(it0, load_req(it0), sMeta[0]);
+    if (producer && it1st >= 0) qn = load_req(it1st);
+    __syncthreads();
+  }
+  if (tid == kRowsProducer && it0 >= 0) issue_rows(0, it0, sMeta[0][1], sMeta[0][3]);
 
   const int c = lane & (LPR - 1);
   const int rg = lane / LPR;
@@ -899,17 +962,21 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   // has finished reading the buffer.
   int pend_it = -1, pend_rows = 0, pend_prev = 0;  // rows producer: copy deferred to the item's end
 
-  for (int k = 0;; ++k) {
-    const int it = blockIdx.x + k * gridDim.x;
-    if (it >= n_items) break;
+  for (int k = 0, it = it0; it >= 0; ++k, it = next_item(it)) {
     const int mi = k & 1;                                  // sMeta slot
     const int s = one_stage ? 0 : mi;                      // rows stage
     const uint32_t qpar = one_stage ? k & 1 : (k >> 1) & 1;  // phase of barQ[s] for this item
     // the arrive that completes each phase releases the producer's sMeta write
     const bool late = !(mbar_wait(&barS, k & 1) && mbar_wait(&barQ[s], qpar));
     if (__syncthreads_or(late)) {
+      // Nothing of this item or later ones is written.  The copies in flight
+      // are this item's (its successor's are issued only after this wait):
+      // a second bounded wait lets a slow one land before the CTA leaves.
+      // The limit is far beyond a copy's microseconds, so only a barrier
+      // whose declared bytes were never issued still reads incomplete here,
+      // and such a barrier has no copy in flight.
       if (tid == 0) flag(p.status, GDN_STATUS_TIMEOUT);
-      mbar_wait(&barS, k & 1);  // bounded: let copies still in flight land before leaving
+      mbar_wait(&barS, k & 1);
       mbar_wait(&barQ[s], qpar);
       return;
     }
@@ -932,10 +999,10 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     __syncthreads();  // the state buffer is free: request the next item
     // On its last item the CTA lets the next call's prologue launch, so that
     // prologue's blocks take the SMs as CTAs leave and warm their inputs.
-    if (it + gridDim.x >= n_items) pdl_trigger();
+    const int it1 = next_item(it);
+    if (it1 < 0) pdl_trigger();
     if (producer) {
-      const int it1 = it + gridDim.x;
-      if (it1 < n_items) {
+      if (it1 >= 0) {
         fence_proxy_async();  // the reads above happen before the bulk copies overwrite the buffers
         int m[4];
         meta(it1, qn, m);  // loaded an item ago
@@ -955,7 +1022,8 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
             pend_prev = m[3];
           }
         }
-        if (it1 + gridDim.x < n_items) qn = load_req(it1 + gridDim.x);  // in flight while this item computes
+        const int it2 = next_item(it1);
+        if (it2 >= 0) qn = load_req(it2);  // in flight while this item computes
       }
     }
     if (!busy) continue;
@@ -1291,9 +1359,9 @@ int launch_rows(const Params& p, cudaStream_t st) {
     c = last;
   }
   const long long items = (long long)p.B * p.H_v * p.slices;
-  const int grid = (int)(items < c.ctas ? items : c.ctas);
-  return c.stages == 2 ? launch(rows_kernel<DK, MODE, 2>, dim3(grid), dim3(Gm::NT), c.smem, st, p)
-                       : launch(rows_kernel<DK, MODE, 1>, dim3(grid), dim3(Gm::NT), c.smem, st, p);
+  const long long grid = items < c.ctas ? items : c.ctas;
+  return c.stages == 2 ? launch(rows_kernel<DK, MODE, 2>, dim3((unsigned)grid), dim3(Gm::NT), c.smem, st, p)
+                       : launch(rows_kernel<DK, MODE, 1>, dim3((unsigned)grid), dim3(Gm::NT), c.smem, st, p);
 }
 
 template <int MODE>
@@ -1339,6 +1407,11 @@ int run_mode(const Params& p, int in_dtype, cudaStream_t st) {
 }
 
 inline bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+// [a, a + na) and [b, b + nb) share a byte (empty ranges share none)
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
 
 inline int rows_per_cta(int d_k) { return d_k >= 32 ? Geo<32>::DVS : Geo<16>::DVS; }
 
@@ -1354,7 +1427,7 @@ int check_shape(const gdn_args* a) {
   if (a->B < 0 || a->R < 1 || a->H_qk < 1 || a->H_v < 1 || a->d_k < 1 || a->d_v < 1 || a->W < 1 ||
       a->pool_slots < 1)
     return GDN_ERR_INVALID_ARG;
-  if ((a->flags & ~GDN_FLAG_RAW_GATING) != 0) return GDN_ERR_INVALID_ARG;
+  if ((a->flags & ~(GDN_FLAG_RAW_GATING | GDN_FLAG_STATE_STABLE)) != 0) return GDN_ERR_INVALID_ARG;
   if (a->in_dtype != GDN_DTYPE_BF16 && a->in_dtype != GDN_DTYPE_F32) return GDN_ERR_UNSUPPORTED;
   if (a->W != kW || a->R > kMaxR) return GDN_ERR_UNSUPPORTED;
   if (a->d_k != 16 && a->d_k != 32 && a->d_k != 64 && a->d_k != 128) return GDN_ERR_UNSUPPORTED;
@@ -1444,6 +1517,7 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.wgh = p.wqk ? p.wqk + off_gh : nullptr;
   p.status = a->status;
   p.raw_gating = (a->flags & GDN_FLAG_RAW_GATING) != 0;
+  p.early = (a->flags & GDN_FLAG_STATE_STABLE) != 0;
   p.A_log = p.raw_gating ? a->A_log : nullptr;
   p.xp = nullptr;
   p.n_prev = p.acc_prev = nullptr;
@@ -1503,6 +1577,15 @@ int run_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream) {
     if (!aligned(prev->x, 16) || !aligned(prev->n_rows, 4) || !aligned(prev->accept_len, 4) ||
         !aligned(prev->carry, 16))
       return GDN_ERR_MISALIGNED;
+    // The previous call's carry and rows must survive until this call has
+    // read them, while it writes its own: the two carries, and the two x
+    // blocks, are different buffers (double-buffered across steps).
+    const size_t esz = cur->in_dtype == GDN_DTYPE_BF16 ? 2 : 4;
+    const size_t xrow = (size_t)cur->B * (size_t)p.C * esz;
+    if (overlaps(cur->carry, sizeof(float) * carry_floats(cur, cur->R, nullptr, nullptr), prev->carry,
+                 sizeof(float) * carry_floats(cur, prev->R, nullptr, nullptr)) ||
+        overlaps(cur->x, xrow * cur->R, prev->x, xrow * prev->R))
+      return GDN_ERR_INVALID_ARG;
     carry_floats(cur, prev->R, &ok, &oa);
     p.pcu = static_cast<const float*>(prev->carry);
     p.pck = p.pcu + ok;
@@ -1560,6 +1643,14 @@ GDN_API size_t gdn_carry_bytes(const gdn_args* args) {
 GDN_API int gdn_verify_deferred(const gdn_args* cur, const gdn_prev_rows* prev, void* stream) {
   return run_deferred(cur, prev, stream);
 }
+
+#ifdef GDN_TEST_HOOKS
+// Test builds only: make the state copy of rows-kernel item `item` of later
+// calls be declared but never issued (-1 restores normal copies).
+GDN_API int gdn_test_drop_state_copy(int item) {
+  return cudaMemcpyToSymbol(g_test_drop_item, &item, sizeof(int)) == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+#endif
 
 GDN_API const char* gdn_strerror(int code) {
   switch (code) {

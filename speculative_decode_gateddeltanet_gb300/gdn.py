@@ -15,9 +15,10 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libgdnspec.so"
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
 STATIC_WORK_BYTES = 32 << 20
-STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT = 1, 2, 4
+STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT, STATUS_TIMEOUT = 1, 2, 4, 8
 BF16, F32 = 0, 1
 FLAG_RAW_GATING = 1
+FLAG_STATE_STABLE = 2  # caller's promise: nothing still running writes this call's slots, slot_ids, n_rows
 REPLAY, SNAPSHOT = 0, 1
 
 _I32, _F32, _P = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
@@ -149,13 +150,16 @@ def gdn_verify_deferred(args: GdnArgs, prev: GdnPrevRows | None, stream=None) ->
 
 def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_qk: int,
               accept_len=None, o=None, scratch_S=None, scratch_cs=None, work=None,
-              status=None, scale: float | None = None, l2_eps: float = 1e-6, A_log=None, carry=None) -> GdnArgs:
+              status=None, scale: float | None = None, l2_eps: float = 1e-6, A_log=None, carry=None,
+              state_stable: bool = False) -> GdnArgs:
     """Fill a GdnArgs from tensors laid out as ``include/gdnspec.h`` states.
 
     Shapes are read from x [B][R][C], ssm_state [P][H_v][d_v][d_k] and
     conv_w [C][W]; the tensors must stay alive while the call runs.  With
     A_log given, g and beta are the raw gating projections (the raw-gating
-    flag is set)."""
+    flag is set).  state_stable sets GDN_FLAG_STATE_STABLE: the caller
+    promises that no kernel still running on the stream writes this call's
+    slots, slot_ids or n_rows, so the call may fetch state early."""
     B, R, _ = x.shape
     P, H_v, d_v, d_k = ssm_state.shape
     W = conv_w.shape[1]
@@ -168,7 +172,7 @@ def make_args(*, x, g, beta, conv_w, conv_state, ssm_state, slot_ids, n_rows, H_
     return GdnArgs(
         B=B, R=R, H_qk=H_qk, H_v=H_v, d_k=d_k, d_v=d_v, W=W, pool_slots=P, in_dtype=dt,
         scale=d_k ** -0.5 if scale is None else scale, l2_eps=l2_eps,
-        flags=0 if A_log is None else FLAG_RAW_GATING,
+        flags=(0 if A_log is None else FLAG_RAW_GATING) | (FLAG_STATE_STABLE if state_stable else 0),
         x=_ptr(x), g=_ptr(g), beta=_ptr(beta), conv_w=_ptr(conv_w), conv_state=_ptr(conv_state),
         ssm_state=_ptr(ssm_state), slot_ids=_ptr(slot_ids), n_rows=_ptr(n_rows),
         accept_len=_ptr(accept_len), o=_ptr(o), scratch_S=_ptr(scratch_S),
@@ -182,7 +186,8 @@ class DeviceLayer:
     Built from a dict of CPU tensors (the layout ``inputs.make_layer`` uses).
     ``o`` is filled with NaN so rows a call must not write stay visibly
     untouched; ``status`` starts at zero; ``work`` is sized by the library.
-    ``carry`` (None until set) is passed as the call's carry for deferred calls."""
+    ``carry`` (None until set) is passed as the call's carry for deferred calls;
+    ``state_stable`` (False until set) sets GDN_FLAG_STATE_STABLE on the call."""
 
     KEYS = ("x", "g", "beta", "conv_w", "conv_state", "ssm_state", "slot_ids", "n_rows", "accept_len")
 
@@ -205,6 +210,7 @@ class DeviceLayer:
             self.scratch_cs = torch.empty((s.B, s.R, s.C, s.W - 1), dtype=self.x.dtype, device=device)
         self.scale, self.l2_eps = scale, l2_eps
         self.carry = None
+        self.state_stable = False
         self.work = None
         self.work = torch.empty(work_bytes(self.args()) // 4, dtype=torch.float32, device=device)
 
@@ -214,7 +220,8 @@ class DeviceLayer:
                          slot_ids=self.slot_ids, n_rows=self.n_rows, accept_len=self.accept_len,
                          o=self.o, scratch_S=self.scratch_S, scratch_cs=self.scratch_cs,
                          work=self.work, status=self.status, H_qk=self.spec.H_qk,
-                         scale=self.scale, l2_eps=self.l2_eps, A_log=self.A_log, carry=self.carry)
+                         scale=self.scale, l2_eps=self.l2_eps, A_log=self.A_log, carry=self.carry,
+                         state_stable=self.state_stable)
 
 
 def greedy_accept(logits, drafts, n_rows, target, accept_len, status=None, stream=None) -> GdnAcceptArgs:

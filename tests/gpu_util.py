@@ -67,6 +67,18 @@ def o_error(o_gpu: np.ndarray, o_ref: np.ndarray, valid: np.ndarray) -> float:
     return float(np.abs(o_gpu[valid] - ref).max() / np.abs(ref).max())
 
 
+def o_error_per_head(o_gpu: np.ndarray, o_ref: np.ndarray, valid: np.ndarray) -> float:
+    """Worst, over the valid (request, row, value head) triples, of
+    max |o - o_ref| / max |o_ref| within that head's d_v outputs: the margin
+    a single small head has, beside the whole-call figure the bar is stated
+    on.  Heads whose reference is exactly zero are skipped."""
+    ref = o_ref[valid]  # [n][H_v][d_v]
+    den = np.abs(ref).max(axis=-1)
+    num = np.abs(o_gpu[valid] - ref).max(axis=-1)
+    ok = den > 0
+    return float((num[ok] / den[ok]).max()) if ok.any() else 0.0
+
+
 def check_against_oracle(layer: dict, dev, ref: dict, *, commit: bool, check_o: bool = True):
     """o within O_TOL on valid rows and untouched (NaN) elsewhere; committed
     slots within S_TOL and their conv window bit-exact; every other slot
@@ -76,6 +88,9 @@ def check_against_oracle(layer: dict, dev, ref: dict, *, commit: bool, check_o: 
     o_err = 0.0
     if check_o:
         o_err = o_error(o, ref["o"], valid)
+        head_err = o_error_per_head(o, ref["o"], valid)
+        print(f"[parity] {layer['spec'].name}: o error {o_err:.2e} of the call's max |o|; "
+              f"worst single (request, row, head) {head_err:.2e} of its own max |o|")
         assert o_err <= O_TOL, f"o max relative error {o_err:.3e}"
         assert np.isnan(o[~valid]).all(), "rows outside the valid set were written"
     S_gpu = dev.ssm_state.cpu()

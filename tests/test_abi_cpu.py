@@ -84,7 +84,7 @@ CASES = [
     ("d_v not a multiple of the block rows", dict(d_v=48), 2),
     ("H_v % H_qk", dict(H_v=24), 2),
     ("dtype", dict(in_dtype=7), 2),
-    ("unknown flag", dict(flags=2), 1),
+    ("unknown flag", dict(flags=4), 1),
     ("raw gating without A_log", dict(flags=1), 1),
     ("misaligned A_log", dict(flags=1, A_log=FAKE + 2), 3),
     ("negative eps", dict(l2_eps=-1.0), 1),
@@ -191,8 +191,11 @@ def test_greedy_accept_empty_batch_is_a_no_op(cuda_lib):
     assert cuda_lib._lib.gdn_greedy_accept(ctypes.byref(a), None) == cuda_lib.OK
 
 
+PREV_X, PREV_CARRY = 4 << 20, 8 << 20  # the pending rows' stand-ins, clear of every FAKE range
+
+
 def good_prev(gdn, **over):
-    p = gdn.GdnPrevRows(R=4, x=FAKE, n_rows=FAKE, accept_len=FAKE, carry=FAKE)
+    p = gdn.GdnPrevRows(R=4, x=PREV_X, n_rows=FAKE, accept_len=FAKE, carry=PREV_CARRY)
     for k, v in over.items():
         setattr(p, k, v)
     return p
@@ -204,9 +207,14 @@ DEFERRED_CASES = [
     ("null pending x", dict(), dict(x=None), 1),
     ("null pending accept_len", dict(), dict(accept_len=None), 1),
     ("null pending carry", dict(), dict(carry=None), 1),
-    ("misaligned pending x", dict(), dict(x=FAKE + 2), 3),
+    ("misaligned pending x", dict(), dict(x=PREV_X + 2), 3),
     ("misaligned pending n_rows", dict(), dict(n_rows=FAKE + 1), 3),
-    ("misaligned pending carry", dict(), dict(carry=FAKE + 4), 3),
+    ("misaligned pending carry", dict(), dict(carry=PREV_CARRY + 4), 3),
+    # a step reads the previous step's carry and rows while writing its own: no shared bytes
+    ("carry out is the pending carry", dict(carry=PREV_CARRY), dict(), 1),
+    ("carry out overlaps the pending carry", dict(carry=PREV_CARRY + 4096), dict(), 1),
+    ("x is the pending x", dict(x=PREV_X), dict(), 1),
+    ("x overlaps the pending x", dict(x=PREV_X - 65536), dict(), 1),
     ("null carry out", dict(carry=None), dict(), 1),
     ("misaligned carry out", dict(carry=FAKE + 8), dict(), 3),
     ("null o", dict(o=None), dict(), 1),
@@ -220,6 +228,19 @@ def test_deferred_rejects_bad_arguments(cuda_lib, what, cur, prev, code):
     a, p = good_args(cuda_lib, **{"carry": FAKE, **cur}), good_prev(cuda_lib, **prev)
     rc = cuda_lib._lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(p), None)
     assert rc == code, (what, cuda_lib.strerror(rc))
+
+
+def test_deferred_overlap_check_passes_distinct_buffers(cuda_lib):
+    """Control for the overlap cases: the same arguments with distinct
+    buffers get past every host check and fail only at the launch, which
+    needs a device.  Run only where there is none (the stand-in addresses
+    must never reach a real GPU)."""
+    import torch
+
+    if torch.cuda.is_available() or torch.cuda.device_count() > 0:
+        pytest.skip("launch-reaching control runs only without a CUDA device")
+    a, p = good_args(cuda_lib, carry=FAKE), good_prev(cuda_lib)
+    assert cuda_lib._lib.gdn_verify_deferred(ctypes.byref(a), ctypes.byref(p), None) == cuda_lib.ERR_LAUNCH
 
 
 def test_deferred_empty_batch_and_no_pending_rows(cuda_lib):

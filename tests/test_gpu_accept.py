@@ -82,3 +82,30 @@ def test_device_accept_feeds_the_commit():
     ref = oracle.verify_commit(dict(layer, accept_len=torch.from_numpy(acc_want.astype(np.int32))))
     check_against_oracle(dict(layer, accept_len=torch.from_numpy(acc_want.astype(np.int32))), dev, ref, commit=True)
     assert int(dev.status.item()) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_nan_and_infinite_rows(dtype):
+    """Rows with NaN logits against the oracle: NaN never wins, a row of only
+    NaN gives token 0, a NaN at the planted maximum moves the choice to the
+    largest remaining value; a row of only -inf gives token 0 (lowest index
+    among equal values)."""
+    case = make_accept_case(6, 3, 512, seed=21, dtype=dtype)
+    case["n_rows"] = torch.full((6,), 3, dtype=torch.int32)
+    lg = case["logits"].float()
+    planted = case["planted_target"]
+    lg[0, 0, :] = float("nan")                       # every logit NaN
+    lg[1, 1, 0] = float("nan")                       # NaN at index 0
+    lg[2, 0, int(planted[2, 0])] = float("nan")      # NaN where the maximum was planted
+    lg[3, 2, ::2] = float("nan")                     # NaN at every even index
+    lg[4, 1, :] = float("-inf")                      # every logit -inf
+    lg[5, 0, :] = float("nan")
+    lg[5, 0, 300] = float("-inf")                    # one -inf among NaN: it wins
+    case["logits"] = lg.to(case["logits"].dtype)
+    target, acc, status = run(case)
+    ref = oracle.greedy_accept(case)
+    assert status == 0
+    assert np.array_equal(target, ref["target"]) and np.array_equal(acc, ref["accept_len"])
+    assert target[0, 0] == 0 and target[4, 1] == 0 and target[5, 0] == 300
+    assert target[2, 0] != planted[2, 0]
+

@@ -1,13 +1,16 @@
 """CUDA-graph capture of whole verify/commit sequences through the C ABI: the
 library allocates nothing and never synchronises, so a captured multi-layer
 step replays to the same bits as the same calls launched eagerly (the
-pages' capture-safe verify with no device-to-host sync)."""
+pages' capture-safe verify with no device-to-host sync), and the replayed
+results match the oracle run on the same sequence of calls under the stated
+tolerances."""
 from __future__ import annotations
 
 import pytest
 import torch
 
-from gpu_util import bits
+import oracle
+from gpu_util import bits, check_against_oracle
 from speculative_decode_gateddeltanet_gb300.inputs import STACK, SWEEP, make_layer, workload_layers
 
 pytestmark = pytest.mark.gpu
@@ -39,13 +42,18 @@ def _same(a, b):
         assert int(x.status.item()) == int(y.status.item()) == 0
 
 
-@pytest.mark.parametrize("mode", ["fused", "replay"])
-def test_captured_stack_replays_to_eager_bits(mode):
+@pytest.mark.parametrize("mode,stable", [("fused", False), ("replay", False), ("fused", True), ("replay", True)])
+def test_captured_stack_replays_to_eager_bits(mode, stable):
+    """Six stack layers captured as one graph (optionally with
+    GDN_FLAG_STATE_STABLE, as the benchmark runs them), replayed twice from
+    the same buffers: eager bits each time, and the oracle's results."""
     from speculative_decode_gateddeltanet_gb300 import gdn
 
     layers = _layers(STACK, layers=6)
     eager = [gdn.DeviceLayer(layer, "cuda") for layer in layers]
     graphed = [gdn.DeviceLayer(layer, "cuda") for layer in layers]
+    for d in eager + graphed:
+        d.state_stable = stable
     stream = torch.cuda.Stream()
 
     def step(devs, args):
@@ -75,6 +83,8 @@ def test_captured_stack_replays_to_eager_bits(mode):
         g.replay()
         torch.cuda.synchronize()
         _same(eager, graphed)
+    for layer, d in zip(layers, graphed):
+        check_against_oracle(layer, d, oracle.verify_commit(layer), commit=True)
 
 
 def test_captured_step_sequence_matches_eager_steps():
@@ -100,6 +110,13 @@ def test_captured_step_sequence_matches_eager_steps():
         g.replay()
     torch.cuda.synchronize()
     _same([eager], [graphed])
+    # the oracle's three steps, each starting from the pools the step before committed
+    pools = {"conv_state": layer["conv_state"], "ssm_state": layer["ssm_state"]}
+    for _ in range(3):
+        ref = oracle.verify_commit(dict(layer, **pools))
+        pools = {"conv_state": torch.from_numpy(ref["conv_state"]).to(layer["conv_state"].dtype),
+                 "ssm_state": torch.from_numpy(ref["ssm_state"])}  # the oracle's chain stays in fp64
+    check_against_oracle(layer, graphed, ref, commit=True)
 
 
 def test_captured_deferred_steps_match_eager():

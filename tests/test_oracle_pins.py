@@ -13,7 +13,7 @@ Pinned:
   * verify-only leaves the slots bitwise untouched [FreeToken #828, Design]
   * conv window: tap W-1 on the newest row, committed window = last W-1 entries
     of [history | accepted rows] [FreeToken #844, Flash-Next target verify;
-    Tests, "the conv commit restores the window one column early"]
+    Tests: a mutation that shifts the committed window by one column]
   * the delta rule, decay, write strength, scale, L2 norm, SiLU: closed form
     and special cases (beta=0 pure decay, beta=1 exact write S k = v,
     orthonormal keys keep every written value)
