@@ -31,8 +31,9 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from speculative_decode_gateddeltanet_gb300.inputs import (CONFIGS, RAGGED, STACK, deferred_bytes,  # noqa: E402
-                                                           make_layer, make_step, spec_bytes, workload_layers)
+from speculative_decode_gateddeltanet_gb300.inputs import (CONFIGS, RAGGED, SINGLE, STACK, SWEEP,  # noqa: E402
+                                                           deferred_bytes, make_layer, make_step, spec_bytes,
+                                                           workload_layers)
 
 METRIC = "GDN verify+commit verified rows/sec and achieved HBM GB/s (% of peak), 1 GB300"
 UNIT = "rows/s"
@@ -48,15 +49,16 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(workload: str, mode: str):
-    """dram bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    """(dram bytes read, dram bytes written) in one launch of the dominant
+    kernel, from the committed ncu summary, if it was taken on the current
+    kernel source; else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     h = kernel_source_hash()
     for line in open(TRAFFIC_FILE):
         parts = line.split()
-        if len(parts) == 4 and not line.startswith("#") and parts[:3] == [workload, mode, h]:
-            return float(parts[3])
+        if len(parts) == 5 and not line.startswith("#") and parts[:3] == [workload, mode, h]:
+            return float(parts[3]), float(parts[4])
     return None
 
 
@@ -157,6 +159,14 @@ def build_stack(layers: int, device: str, batch: int | None = None, workload: st
     if workload == "ragged":  # B=256 requests of 2, 4 or 9 rows, 64 value heads, 10 % inactive
         base = CONFIGS[RAGGED]
         specs = [(replace(base, name=f"ragged-{layers}L-B256-k1_3_8"), 4000 + i) for i in range(layers)]
+    elif workload == "single":  # the single-layer B=1, k=3 call, as distinct layers so L2 cannot hold them
+        base = CONFIGS[SINGLE]
+        specs = [(replace(base, name=f"qwen35-{layers}L-B1-k3"), 1000 + i) for i in range(layers)]
+    elif workload == "sweep":  # the batch sweep's k=2 calls (2B-slot pools), at --batch B, as distinct layers
+        b = 16 if batch is None else batch
+        base = replace(CONFIGS[SWEEP], B=b)
+        specs = [(replace(base, name=f"qwen35-{layers}L-B{b}-k2"), 2000 + 100 * b + i) for i in range(layers)]
+        batch = None
     else:
         specs = workload_layers(STACK, layers=layers)
     for spec, seed in specs:
@@ -339,6 +349,7 @@ def run_cuda(args, rank, ws, local):
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), ws) / e2e_steps
 
     peak, peak_kind = hbm_peak()
+    traffic = measured_traffic(spec.name, args.mode)
     per_launch_bytes = bytes_per_step / len(cargs)
     launch_s = ms_step / 1e3 / calls_per_step
     achieved = (per_launch_bytes / launch_s / 1e9 if args.mode in ("fused", "deferred")
@@ -359,7 +370,13 @@ def run_cuda(args, rank, ws, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "kernel": "rows_kernel<128, %s>" % args.mode,
-                     "traffic": measured_traffic(spec.name, args.mode),
+                     "traffic": None if traffic is None else traffic[0] + traffic[1],
+                     "traffic_read": None if traffic is None else traffic[0],
+                     "traffic_write": None if traffic is None else traffic[1],
+                     "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one rows-kernel launch, "
+                                     "inside its own window: the committed state it writes (2 MiB per request) "
+                                     "stays dirty in L2 and reaches DRAM while later kernels run, so the window "
+                                     "shows its reads (state, staged rows) and almost none of its writes",
                      "algorithmic_bytes_per_launch": round(per_launch_bytes)},
         "e2e": {"value": round(rows_per_step * ws / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -538,9 +555,11 @@ def main(argv=None):
                          "carry and verifies the current ones (gdn_verify_deferred)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layer calls per step (default 36 for the stack, 4 for the ragged batch)")
-    ap.add_argument("--workload", choices=["stack", "ragged"], default="stack",
+    ap.add_argument("--workload", choices=["stack", "ragged", "single", "sweep"], default="stack",
                     help="stack: 36 Qwen3.5-shaped layers at B=16, k=3; ragged: B=256 requests with k in "
-                         "{1,3,8} and 64 value heads (about 1 GB of state per layer)")
+                         "{1,3,8} and 64 value heads (about 1 GB of state per layer); single: the B=1, k=3 "
+                         "call as 36 distinct layers; sweep: the batch sweep's k=2 call at --batch B (2B-slot "
+                         "pools), as 36 distinct layers")
     ap.add_argument("--batch", type=int, default=None, help="requests per layer (default: the workload's 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
