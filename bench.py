@@ -384,7 +384,7 @@ def run_cuda(args, rank, ws, local):
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(host, budget_s=args.cpu_seconds)
     return out
 
 
@@ -446,29 +446,27 @@ def run_accept(args, rank, ws, local):
 
 
 # ------------------------------------------------------------ oracle arm
-def oracle_rows_per_second(budget_s: float, max_layers: int = 36):
-    """Time the oracle on whole layers of the stack until the budget is used."""
+def oracle_rows_per_second(layers: list, budget_s: float):
+    """Time the oracle on one thread over whole layer calls of the workload
+    (cycling over its layers) until the budget is used."""
     import oracle
 
-    rows, secs, layers = 0, 0.0, 0
-    stack = workload_layers(STACK, layers=max_layers)
+    rows, secs, calls = 0, 0.0, 0
     while secs < budget_s:
-        spec, seed = stack[layers % len(stack)]
-        layer = make_layer(spec, seed)
+        layer = layers[calls % len(layers)]
         r = oracle.verify_commit(layer)
         rows += int(layer["n_rows"].clamp(min=0).sum())
         secs += r["seconds"]
-        layers += 1
-    return rows, secs, layers
+        calls += 1
+    return rows, secs, calls
 
 
-def oracle_rows_per_second_threads(budget_s: float, threads: int, n_layers: int = 4):
+def oracle_rows_per_second_threads(layers: list, budget_s: float, threads: int):
     """The oracle over all host cores: each layer call's requests spread over
-    ``threads`` threads (``oracle.verify_commit_threads``), cycling over a few
-    layers of the stack until the wall-time budget is used."""
+    ``threads`` threads (``oracle.verify_commit_threads``), cycling over the
+    given layers until the wall-time budget is used."""
     import oracle
 
-    layers = [make_layer(spec, seed) for spec, seed in workload_layers(STACK, layers=n_layers)]
     rows, secs, calls, used = 0, 0.0, 0, 1
     while secs < budget_s:
         layer = layers[calls % len(layers)]
@@ -487,17 +485,21 @@ def host_threads() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(budget_s: float = 12.0):
-    """The oracle on the host: all cores (the reported value) and one core."""
-    rows1, secs1, layers1 = oracle_rows_per_second(budget_s / 2)
-    rows, secs, calls, used = oracle_rows_per_second_threads(budget_s / 2, host_threads())
+def cpu_baseline(layers: list, budget_s: float = 12.0):
+    """The oracle on the host, on the bench's own host-side layers (the same
+    seeded inputs the GPU ran): all cores (the reported value) and one core,
+    half the budget each, cycling over at most four layers."""
+    layers = layers[:4]
+    spec = layers[0]["spec"]
+    rows1, secs1, calls1 = oracle_rows_per_second(layers, budget_s / 2)
+    rows, secs, calls, used = oracle_rows_per_second_threads(layers, budget_s / 2, host_threads())
     return {"value": round(rows / secs, 1), "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"fp64 C oracle, fused verify+commit, each layer call's 16 requests spread over {used} host "
-                      f"threads: {calls} calls ({rows} rows) cycling over 4 layers of the 36-layer B=16 k=3 stack, "
-                      f"{secs:.1f} s wall",
+            "sample": f"fp64 C oracle, fused verify+commit, each layer call's {spec.B} requests spread over {used} "
+                      f"host threads: {calls} calls ({rows} rows) cycling over {len(layers)} layers of "
+                      f"{spec.name}, {secs:.1f} s wall",
             "one_core": {"value": round(rows1 / secs1, 1), "unit": UNIT, "cores": 1,
-                         "sample": f"single thread, {layers1} whole layer calls ({rows1} rows) cycling over the "
-                                   f"stack, {secs1:.1f} s"}}
+                         "sample": f"single thread, {calls1} whole layer calls ({rows1} rows) of the same layers, "
+                                   f"{secs1:.1f} s"}}
 
 
 def run_reference(args, rank, ws):

@@ -71,8 +71,31 @@ constexpr unsigned kFull = 0xffffffffu;
 // current rows are verified from that state (o, and their own carry).
 enum Mode : int { kFused = 0, kVerify = 1, kVerifySnap = 2, kCommitReplay = 3, kDeferred = 4 };
 
+// Division of 0 <= n < 2^31 by a divisor d >= 1 fixed for the launch, as
+// floor(n m / 2^k) with k = 31 + ceil(log2 d) and m = ceil(2^k / d).  With
+// m d = 2^k + e (0 <= e < d) and n = q d + r, n m / 2^k = q + (r + n e / 2^k) / d,
+// and n e < 2^31 2^ceil(log2 d) = 2^k makes the fraction below 1.  The product
+// is below 2^64 (m < 2^33), so one wide multiply and a shift replace the
+// integer division's reciprocal sequence.
+struct FastDiv {
+  unsigned long long m;
+  int k;
+};
+inline FastDiv make_fastdiv(int d) {
+  int c = 0;
+  while ((1LL << c) < d) ++c;
+  const int k = 31 + c;
+  const unsigned long long two_k = 1ULL << k;
+  return FastDiv{two_k / (unsigned long long)d + (two_k % (unsigned long long)d != 0), k};
+}
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  return (int)(((unsigned long long)(unsigned)n * f.m) >> f.k);
+}
+
 struct Params {
   int B, R, H_qk, H_v, d_k, d_v, P, G, slices;
+  // item it = ((b H_v) + h) slices + sl: divisions by H_v slices, slices and G
+  FastDiv div_hs, div_sl, div_g;
   long long C;
   float scale, eps;
   const void* x;
@@ -117,18 +140,23 @@ struct Params {
 
 __host__ __device__ constexpr int round4(int r) { return (r + 3) & ~3; }
 
-// Lane geometry of the rows kernel for a d_k-column state.
-template <int DK>
+// Lane geometry of the rows kernel for a d_k-column state.  WIDE (d_k = 128
+// only): four warps and 64 state rows per item instead of two warps and 32,
+// so an item's fixed costs (its waits, its copies, the producers' request
+// bookkeeping, the staged q/k rows and tables) are shared by twice the rows.
+template <int DK, bool WIDE = false>
 struct Geo {
+  static_assert(!WIDE || DK == 128, "the wide geometry is for d_k = 128");
   static constexpr int LPR = DK >= 32 ? 8 : 4;   // lanes per state row
   static constexpr int NC4 = DK / (4 * LPR);     // 4-column chunks per lane per row
   static constexpr int RG = 32 / LPR;            // row groups per warp
   static constexpr int M = DK >= 64 ? 4 : 2;     // rows per lane
   static constexpr int ROWS_W = RG * M;          // rows per warp
-  static constexpr int NW = DK == 16 ? 1 : (M == 4 ? 2 : 4);  // warps per CTA
-  static constexpr int DVS = NW * ROWS_W;        // state rows per CTA (32, or 16 at d_k = 16)
+  static constexpr int NW = DK == 16 ? 1 : (WIDE || M == 2 ? 4 : 2);  // warps per CTA
+  static constexpr int DVS = NW * ROWS_W;        // state rows per CTA (32; 16 at d_k = 16; 64 wide)
   static constexpr int NT = NW * 32;
-  static constexpr int MIN_CTAS = NT == 64 ? 8 : (NT == 128 ? 5 : 16);  // resident CTAs per SM the registers must allow
+  // resident CTAs per SM the registers must allow
+  static constexpr int MIN_CTAS = NT == 64 ? 8 : (NT == 128 ? (WIDE ? 4 : 5) : 16);
 };
 
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
@@ -734,9 +762,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
 // so every dot product of the chunk is taken on the chunk's starting state S0
 // in one pass, each state row then runs a short scalar recurrence, and the
 // state is written once (at the commit row, or advanced to the chunk's end).
-template <int DK>
+template <int DK, bool WIDE = false>
 struct Stage {
-  static constexpr int DVS = Geo<DK>::DVS;
+  static constexpr int DVS = Geo<DK, WIDE>::DVS;
   __host__ __device__ static int rows_floats(int R) { return R * 2 * DK + R * DVS + R * 4 + gram_floats(R); }
   // deferred mode: a previous call's carry rows, [Rp][DVS] u | [Rp][DK] k^ | [Rp4] exp(g)
   __host__ __device__ static int carry_floats(int Rp) { return Rp * DVS + Rp * DK + round4(Rp); }
@@ -794,10 +822,10 @@ __device__ __forceinline__ int lane_of_row(int m) {
 
 // STAGES: buffers for an item's staged rows, 2 (the next item's rows land
 // while this one computes) or 1 (they land once this item is done with them).
-template <int DK, int MODE, int STAGES>
-__global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(const Params p) {
+template <int DK, int MODE, int STAGES, bool WIDE>
+__global__ void __launch_bounds__(Geo<DK, WIDE>::NT, Geo<DK, WIDE>::MIN_CTAS) rows_kernel(const Params p) {
   constexpr bool one_stage = STAGES == 1;
-  using Gm = Geo<DK>;
+  using Gm = Geo<DK, WIDE>;
   constexpr int LPR = Gm::LPR, NC4 = Gm::NC4, RG = Gm::RG, M = Gm::M;
   constexpr int DVS = Gm::DVS, ROWS_W = Gm::ROWS_W;
   constexpr int NP = 2 * NC4;  // column pairs per lane per row
@@ -812,15 +840,9 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   const int n_items = p.B * p.H_v * p.slices;
   const int R = p.R;
   const int Rp = MODE == kDeferred ? p.Rp : 0;
-  // The CTA's k-th item (-1 past its last).  Full rounds k < Q give CTA j item
-  // k G + j.  The partial last round's E < G items go to the CTAs j with
-  // floor((j+1) E / G) > floor(j E / G): an even share of every run of
-  // consecutive CTAs.  CTAs that become resident together tend to share SMs,
-  // so handing the partial round to the first E CTAs loads some SMs with two
-  // items per CTA and leaves others with one; spread, each SM gets its share.
   // The CTA's item after item `it` (-1: none): CTA j runs items j, j + G, j + 2G, ...
   auto next_item = [&](int it) -> int { return it + (int)gridDim.x < n_items ? it + (int)gridDim.x : -1; };
-  const int rfl = Stage<DK>::rows_floats(R) + Stage<DK>::carry_floats(Rp);
+  const int rfl = Stage<DK, WIDE>::rows_floats(R) + Stage<DK, WIDE>::carry_floats(Rp);
   extern __shared__ __align__(16) float smem[];
   float* const stS = smem;  // [DVS][DK] state slice of the next item
   auto stQK = [&](int s) { return smem + DVS * DK + (size_t)s * rfl; };  // [R][2 DK]  scale*q^ | k^
@@ -841,7 +863,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     int n, slot, a, np;  // np: the previous call's rows (deferred mode), a then its accepted drafts
   };
   auto load_req = [&](int it) {
-    const int b = it / (p.H_v * p.slices);
+    const int b = fdiv(it, p.div_hs);
     Req q;
     q.n = p.n_rows[b];
     q.slot = p.slot_ids[b];
@@ -856,7 +878,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
   };
   // item it's request data -> its row of sMeta; reports a bad request once per request
   auto meta = [&](int it, const Req& q, int* m) {
-    const int hs = it % (p.H_v * p.slices);
+    const int hs = it - fdiv(it, p.div_hs) * p.H_v * p.slices;
     int report, crow, off = 0;
     m[0] = q.slot;
     if (MODE == kDeferred) {  // rows = the current rows only; off previous rows are committed first
@@ -873,7 +895,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       mbar_arrive(&barS);
       return;
     }
-    const int b = it / (p.H_v * p.slices);
+    const int b = fdiv(it, p.div_hs);
     const int hs = it - b * p.H_v * p.slices;  // h * slices + sl
     mbar_expect_tx(&barS, kSBytes);
 #ifdef GDN_TEST_HOOKS
@@ -889,10 +911,10 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
       mbar_arrive(&barQ[s]);
       return;
     }
-    const int b = it / (p.H_v * p.slices);
+    const int b = fdiv(it, p.div_hs);
     const int hs = it - b * p.H_v * p.slices;
-    const int h = hs / p.slices;
-    const int hq = h / p.G;
+    const int h = fdiv(hs, p.div_sl);
+    const int hq = fdiv(h, p.div_g);
     mbar_expect_tx(&barQ[s], rb + cb);
     if (rows > 0) {
       bulk_load(stQK(s), p.wqk + ((size_t)b * p.H_qk + hq) * R * 2 * DK, rows * 2 * DK * sizeof(float), &barQ[s]);
@@ -929,7 +951,7 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
         // caller promised nothing in flight writes them or the state); the
         // slice is fetched whenever the request could need it, and what the
         // item does with it is decided after the wait.
-        const int b = it0 / (p.H_v * p.slices);
+        const int b = fdiv(it0, p.div_hs);
         const int slot = p.slot_ids[b], n = p.n_rows[b];
         const bool need = slot >= 0 && slot < p.P && n >= 0 && n <= p.R && (n > 0 || MODE == kDeferred);
         issue_state(it0, slot, need ? 1 : 0);
@@ -1028,9 +1050,9 @@ __global__ void __launch_bounds__(Geo<DK>::NT, Geo<DK>::MIN_CTAS) rows_kernel(co
     }
     if (!busy) continue;
 
-    const int b = it / (p.H_v * p.slices);
+    const int b = fdiv(it, p.div_hs);
     const int hs = it - b * p.H_v * p.slices;
-    const int h = hs / p.slices, sl = hs - h * p.slices;
+    const int h = fdiv(hs, p.div_sl), sl = hs - h * p.slices;
     const float* sQK = stQK(s);
     const float* sV = stV(s);
     const float* sSC = stSC(s);
@@ -1315,16 +1337,16 @@ int setup_kernel(Kernel kernel, size_t max_smem, std::atomic<unsigned long long>
 
 // Persistent grid of the rows kernel: as many CTAs as fit at once (at most one
 // per item).
-template <int DK, int MODE>
+template <int DK, int MODE, bool WIDE>
 int launch_rows(const Params& p, cudaStream_t st) {
-  using Gm = Geo<DK>;
+  using Gm = Geo<DK, WIDE>;
   const int Rp = MODE == kDeferred ? p.Rp : 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_LAUNCH;
   static std::atomic<unsigned long long> set1{0}, set2{0};
   const int max_rp = MODE == kDeferred ? kMaxR : 0;
-  int rc = setup_kernel(rows_kernel<DK, MODE, 1>, Stage<DK>::bytes(kMaxR, max_rp, 1), set1, dev);
-  if (rc == GDN_OK) rc = setup_kernel(rows_kernel<DK, MODE, 2>, Stage<DK>::bytes(kMaxR, max_rp, 2), set2, dev);
+  int rc = setup_kernel(rows_kernel<DK, MODE, 1, WIDE>, Stage<DK, WIDE>::bytes(kMaxR, max_rp, 1), set1, dev);
+  if (rc == GDN_OK) rc = setup_kernel(rows_kernel<DK, MODE, 2, WIDE>, Stage<DK, WIDE>::bytes(kMaxR, max_rp, 2), set2, dev);
   if (rc != GDN_OK) return rc;
   // Double-buffered rows staging unless one buffer lets at least a quarter
   // more CTAs be resident (long requests): measured, one more CTA per SM
@@ -1341,11 +1363,11 @@ int launch_rows(const Params& p, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (last.dev != dev || last.R != p.R || last.Rp != Rp) {
-      const size_t smem2 = Stage<DK>::bytes(p.R, Rp, 2), smem1 = Stage<DK>::bytes(p.R, Rp, 1);
+      const size_t smem2 = Stage<DK, WIDE>::bytes(p.R, Rp, 2), smem1 = Stage<DK, WIDE>::bytes(p.R, Rp, 1);
       int per2 = 0, per1 = 0, sms = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, rows_kernel<DK, MODE, 2>, Gm::NT, smem2) !=
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, rows_kernel<DK, MODE, 2, WIDE>, Gm::NT, smem2) !=
               cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, rows_kernel<DK, MODE, 1>, Gm::NT, smem1) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, rows_kernel<DK, MODE, 1, WIDE>, Gm::NT, smem1) !=
               cudaSuccess ||
           cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per1 < 1)
         return GDN_ERR_LAUNCH;
@@ -1360,21 +1382,23 @@ int launch_rows(const Params& p, cudaStream_t st) {
   }
   const long long items = (long long)p.B * p.H_v * p.slices;
   const long long grid = items < c.ctas ? items : c.ctas;
-  return c.stages == 2 ? launch(rows_kernel<DK, MODE, 2>, dim3((unsigned)grid), dim3(Gm::NT), c.smem, st, p)
-                       : launch(rows_kernel<DK, MODE, 1>, dim3((unsigned)grid), dim3(Gm::NT), c.smem, st, p);
+  return c.stages == 2 ? launch(rows_kernel<DK, MODE, 2, WIDE>, dim3((unsigned)grid), dim3(Gm::NT), c.smem, st, p)
+                       : launch(rows_kernel<DK, MODE, 1, WIDE>, dim3((unsigned)grid), dim3(Gm::NT), c.smem, st, p);
 }
 
 template <int MODE>
 int dispatch_rows(const Params& p, cudaStream_t st) {
   switch (p.d_k) {
     case 16:
-      return launch_rows<16, MODE>(p, st);
+      return launch_rows<16, MODE, false>(p, st);
     case 32:
-      return launch_rows<32, MODE>(p, st);
+      return launch_rows<32, MODE, false>(p, st);
     case 64:
-      return launch_rows<64, MODE>(p, st);
+      return launch_rows<64, MODE, false>(p, st);
     default:
-      return launch_rows<128, MODE>(p, st);
+      if constexpr (MODE != kDeferred)
+        if (p.dvs == Geo<128, true>::DVS) return launch_rows<128, MODE, true>(p, st);
+      return launch_rows<128, MODE, false>(p, st);
   }
 }
 
@@ -1415,6 +1439,55 @@ inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 inline int rows_per_cta(int d_k) { return d_k >= 32 ? Geo<32>::DVS : Geo<16>::DVS; }
 
+#ifdef GDN_TEST_HOOKS
+// Test builds only: the rows per item later calls are forced to (0: chosen by
+// shape; 64: the wide geometry wherever it applies; any other positive value:
+// the two-warp one) and the rows per item the last call chose.
+std::atomic<int> g_test_item_rows{0}, g_test_last_item_rows{0};
+#endif
+
+// Resident CTAs of the two-warp d_k = 128 rows kernel on the current device
+// (8 per SM), read once per device; 0 when it cannot be read.
+int narrow_slots() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  v = Geo<128>::MIN_CTAS * sms;
+  cached[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// State rows per rows-kernel item.  The wide geometry (64 rows, four warps)
+// when d_k = 128, requests have more than 4 rows and its items still
+// outnumber the two-warp kernel's resident CTAs: measured on the ragged
+// B = 256 batch (up to 9 rows) 2.59 M against 2.03 M rows/s, while at 4 rows
+// it is even with the two-warp form and at B = 1 it leaves CTAs idle.  Never
+// for deferred calls, whose carry layout (by slice) must not change between
+// calls of different row counts.
+int rows_per_item(const gdn_args* a, bool wide_ok) {
+  constexpr int kWide = Geo<128, true>::DVS;
+  const bool can_wide = wide_ok && a->d_k == 128 && a->d_v % kWide == 0;
+  int rows = rows_per_cta(a->d_k);
+  if (can_wide && a->R > 4) {
+    const long long items = (long long)a->B * a->H_v * (a->d_v / kWide);
+    const int slots = narrow_slots();
+    if (slots > 0 && items >= slots) rows = kWide;
+  }
+#ifdef GDN_TEST_HOOKS
+  const int forced = g_test_item_rows.load(std::memory_order_relaxed);
+  if (forced == kWide && can_wide)
+    rows = kWide;
+  else if (forced > 0 && forced != kWide)
+    rows = rows_per_cta(a->d_k);
+  g_test_last_item_rows.store(rows, std::memory_order_relaxed);
+#endif
+  return rows;
+}
+
 enum Need : unsigned {
   kNeedRows = 1u,  // x, g, beta, conv_w, work
   kNeedO = 2u,
@@ -1452,7 +1525,7 @@ size_t work_floats(const gdn_args* a, size_t* off_v, size_t* off_sc, size_t* off
   return qk + v + sc + (size_t)a->B * a->H_qk * gram_floats(a->R);
 }
 
-int validate(const gdn_args* a, unsigned need, Params* out) {
+int validate(const gdn_args* a, unsigned need, Params* out, bool wide_ok = false) {
   int rc = check_shape(a);
   if (rc != GDN_OK) return rc;
   if (!std::isfinite(a->scale) || !std::isfinite(a->l2_eps) || a->l2_eps < 0.f) return GDN_ERR_INVALID_ARG;
@@ -1492,7 +1565,11 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.d_v = a->d_v;
   p.P = a->pool_slots;
   p.G = a->H_v / a->H_qk;
-  p.slices = a->d_v / rows_per_cta(a->d_k);
+  p.dvs = rows_per_item(a, wide_ok);
+  p.slices = a->d_v / p.dvs;
+  p.div_hs = make_fastdiv(p.H_v * p.slices);
+  p.div_sl = make_fastdiv(p.slices);
+  p.div_g = make_fastdiv(p.G);
   p.C = 2LL * a->H_qk * a->d_k + (long long)a->H_v * a->d_v;
   p.scale = a->scale;
   p.eps = a->l2_eps;
@@ -1508,7 +1585,6 @@ int validate(const gdn_args* a, unsigned need, Params* out) {
   p.o = a->o;
   p.snapS = a->scratch_S;
   p.snapCs = a->scratch_cs;
-  p.dvs = rows_per_cta(a->d_k);
   size_t off_v = 0, off_sc = 0, off_gh = 0;
   work_floats(a, &off_v, &off_sc, &off_gh);
   p.wqk = static_cast<float*>(a->work);
@@ -1540,7 +1616,7 @@ size_t carry_floats(const gdn_args* a, int R, size_t* off_k, size_t* off_a) {
 
 int run_rows(const gdn_args* args, unsigned need, int mode, void* stream) {
   Params p;
-  const int rc = validate(args, need, &p);
+  const int rc = validate(args, need, &p, true);
   if (rc != GDN_OK || p.B == 0) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (mode) {
@@ -1650,6 +1726,15 @@ GDN_API int gdn_verify_deferred(const gdn_args* cur, const gdn_prev_rows* prev, 
 GDN_API int gdn_test_drop_state_copy(int item) {
   return cudaMemcpyToSymbol(g_test_drop_item, &item, sizeof(int)) == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
+// Test builds only: force the rows per rows-kernel item of later calls (0:
+// chosen by shape; 32: the two-warp geometry; 64: the wide geometry where it
+// applies) and read the rows per item of the last call.
+GDN_API int gdn_test_force_item_rows(int rows) {
+  if (rows != 0 && rows != 32 && rows != 64) return GDN_ERR_INVALID_ARG;
+  g_test_item_rows.store(rows, std::memory_order_relaxed);
+  return GDN_OK;
+}
+GDN_API int gdn_test_last_item_rows() { return g_test_last_item_rows.load(std::memory_order_relaxed); }
 #endif
 
 GDN_API const char* gdn_strerror(int code) {

@@ -18,9 +18,13 @@ def dvs(dk):
     return 16 if dk == 16 else 32
 
 
-@pytest.mark.parametrize("dk", [16, 32, 64, 128])
-def test_rows_kernel_stage_and_copies_are_16_byte_aligned(dk):
-    D = dvs(dk)
+# state rows per item: every d_k's two-warp (or one-warp) geometry, and the
+# four-warp 64-row geometry at d_k = 128
+GEOMETRIES = [(16, 16), (32, 32), (64, 32), (128, 32), (128, 64)]
+
+
+@pytest.mark.parametrize("dk,D", GEOMETRIES)
+def test_rows_kernel_stage_and_copies_are_16_byte_aligned(dk, D):
     for R in range(1, 17):
         rfl = R * 2 * dk + R * D + R * 4 + gram_floats(R)
         for s in (0, 1):
@@ -36,9 +40,13 @@ def test_rows_kernel_stage_and_copies_are_16_byte_aligned(dk):
 
 
 @pytest.mark.parametrize("dk,B,R,Hq,G", list(itertools.product([16, 128], [1, 3], [1, 3, 9, 16], [1, 2], [1, 4])))
-def test_work_regions_are_16_byte_aligned(cuda_lib, dk, B, R, Hq, G):
-    Hv, dv = Hq * G, dvs(dk) * 2
-    slices = dv // dvs(dk)
+@pytest.mark.parametrize("wide", [False, True])
+def test_work_regions_are_16_byte_aligned(cuda_lib, dk, B, R, Hq, G, wide):
+    if wide and dk != 128:
+        pytest.skip("the 64-row geometry is for d_k = 128")
+    D = 64 if wide else dvs(dk)
+    Hv, dv = Hq * G, D * 2
+    slices = dv // D
     qk = B * R * Hq * 2 * dk
     v = B * R * Hv * dv
     sc = B * R * Hv * 4
@@ -51,7 +59,7 @@ def test_work_regions_are_16_byte_aligned(cuda_lib, dk, B, R, Hq, G):
             assert ((b * Hq + hq) * R * 2 * dk) % 4 == 0
             assert ((b * Hq + hq) * gram_floats(R)) % 4 == 0
         for hs in range(Hv * slices):
-            assert ((b * Hv * slices + hs) * R * dvs(dk)) % 4 == 0
+            assert ((b * Hv * slices + hs) * R * D) % 4 == 0
         for h in range(Hv):
             assert ((b * Hv + h) * R * 4) % 4 == 0
     a = cuda_lib.GdnArgs(B=B, R=R, H_qk=Hq, H_v=Hv, d_k=dk, d_v=dv, W=4, pool_slots=1,
