@@ -230,6 +230,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // grid has triggered or exited.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// A relaxed GPU-scope load: well defined even while another grid may be
+// writing the word, so its value can only serve as a guess that is checked
+// against a plain load after the dependency wait.
+__device__ __forceinline__ int ld_relaxed(const int* ptr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 // ---- bulk async copies (TMA, 1-D) into shared memory, tracked by an mbarrier ----
 __device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
@@ -386,6 +395,16 @@ template <typename T, int MODE, int RMAX>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   constexpr bool kCommits = MODE == kFused || MODE == kCommitReplay || MODE == kDeferred;
   constexpr bool kSnap = MODE == kVerifySnap;
+  // Requests of at most 4 rows: the block's loads are issued right after the
+  // wait, together with the request data, so they do not wait for a second
+  // round trip: every row of x and gating the buffers hold, the taps and the
+  // conv window of the request's slot as read before the wait (a guess, since
+  // the kernels ahead may still be writing slot_ids; a block whose request
+  // turns out to use another slot loads that slot's window again).  Longer
+  // requests read the request first and load only its rows: measured, the
+  // early loads' registers cost more blocks in flight than the round trip.
+  constexpr bool kGuess = RMAX <= 4;
+  const int slot_seen = ld_relaxed(p.slot_ids + blockIdx.y);
   // L2 hints for this block's own inputs (its channels of the current rows of
   // x, the slot's conv window and the taps), issued while the call waits for
   // the work before it so the loads after the wait find them in L2.  A hint
@@ -409,9 +428,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
         src = static_cast<const char*>(p.x) + (((size_t)b * p.R + j) * p.C + ch) * sizeof(T);
         bytes = nch * sizeof(T);
       } else if (j == p.R) {
-        const int slot = p.slot_ids[b];
-        if (slot >= 0 && slot < p.P) {
-          src = static_cast<const char*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS * sizeof(T);
+        if (slot_seen >= 0 && slot_seen < p.P) {
+          src = static_cast<const char*>(p.conv_state) + ((size_t)slot_seen * p.C + ch) * kWS * sizeof(T);
           bytes = nch * kWS * sizeof(T);
         }
       } else {
@@ -431,13 +449,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
 
   const int b = blockIdx.y;
-  int slot, a, off, report;
-  const int t_end = request_block<MODE>(p, b, slot, a, off, report);
-  const bool commit = a >= 0;
-  if (t_end == 0) return;  // the rows kernel records bad requests
+  const bool guess_ok = slot_seen >= 0 && slot_seen < p.P;
+  // The request's block of rows (the rows kernel records bad requests).
   // Block rows t < off are the previous call's (deferred mode): they only
   // advance the conv window.  The current rows t >= off are outputs r = t - off.
-  const int n = t_end - off;
+  int slot, a, off, report;
+  auto request = [&]() { return request_block<MODE>(p, b, slot, a, off, report); };
+  int t_end = 0;
+  if constexpr (!kGuess) {  // longer requests: read first, then only their rows loaded
+    t_end = request();
+    if (t_end == 0) return;
+  }
   // gating of current row r for value head h
   auto load_gate = [&](int r, int h, float& gv, float& bv) {
     const size_t i = ((size_t)b * p.R + r) * p.H_v + h;
@@ -459,13 +481,46 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     if (v0 >= p.H_v * p.d_v) return;
     const long long cv = 2LL * p.H_qk * DK + v0;
     const Chunk* wg = reinterpret_cast<const Chunk*>(static_cast<const T*>(p.conv_w) + cv * kW);
-    Chunk* cs = reinterpret_cast<Chunk*>(static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + cv) * kWS);
-    // every load first, so they are all in flight together: the current rows
-    // and (deferred) the last kWS of the previous call's rows 0..off-1
-    Chunk xr[RMAX], xq[kWS];
+    auto window = [&](int sl) {
+      return reinterpret_cast<Chunk*>(static_cast<T*>(p.conv_state) + ((size_t)sl * p.C + cv) * kWS);
+    };
+    // every load first, so they are all in flight together
+    Chunk xr[RMAX], xq[kWS], wc[kW], rc[kWS];
+    auto load_x = [&](int t) {
+      xr[t] = *reinterpret_cast<const Chunk*>(static_cast<const T*>(p.x) + ((size_t)b * p.R + t) * p.C + cv);
+    };
+    if constexpr (kGuess) {  // every row the buffer holds, the taps, the guessed window; then the request
 #pragma unroll
-    for (int t = 0; t < RMAX; ++t)
-      if (t < n) xr[t] = *reinterpret_cast<const Chunk*>(static_cast<const T*>(p.x) + ((size_t)b * p.R + t) * p.C + cv);
+      for (int t = 0; t < RMAX; ++t)
+        if (t < p.R) load_x(t);
+#pragma unroll
+      for (int i = 0; i < kW; ++i) wc[i] = wg[i];
+      if (guess_ok) {
+        const Chunk* g0 = window(slot_seen);
+#pragma unroll
+        for (int i = 0; i < kWS; ++i) rc[i] = g0[i];
+      }
+      t_end = request();
+      if (t_end == 0) return;
+      if (slot != slot_seen) {  // the guess missed: the request's own window
+        const Chunk* w0 = window(slot);
+#pragma unroll
+        for (int i = 0; i < kWS; ++i) rc[i] = w0[i];
+      }
+    } else {  // the request's rows, the taps, its window
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t)
+        if (t < t_end - off) load_x(t);
+#pragma unroll
+      for (int i = 0; i < kW; ++i) wc[i] = wg[i];
+      const Chunk* w0 = window(slot);
+#pragma unroll
+      for (int i = 0; i < kWS; ++i) rc[i] = w0[i];
+    }
+    const bool commit = a >= 0;
+    const int n = t_end - off;
+    Chunk* cs = window(slot);
+    // (deferred) the last kWS of the previous call's rows 0..off-1
     if (MODE == kDeferred) {
 #pragma unroll
       for (int i = 0; i < kWS; ++i) {
@@ -474,11 +529,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
           xq[i] = *reinterpret_cast<const Chunk*>(static_cast<const T*>(p.xp) + ((size_t)b * p.Rp + t) * p.C + cv);
       }
     }
-    Chunk wc[kW], rc[kWS];
-#pragma unroll
-    for (int i = 0; i < kW; ++i) wc[i] = wg[i];
-#pragma unroll
-    for (int i = 0; i < kWS; ++i) rc[i] = cs[i];
     const T* we = reinterpret_cast<const T*>(wc);  // [channel][tap]
     T* re = reinterpret_cast<T*>(rc);               // [channel][window column], oldest first
     float w[VV][kW];
@@ -552,19 +602,57 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   const long long ch =
       tid < DK ? (long long)hq * DK + tid : (long long)p.H_qk * DK + (long long)hq * DK + (tid - DK);
 
-  // gating of the value heads that read this q/k head: loaded now, written at the end
+  // gating of the value heads that read this q/k head, (head, row) pair
+  // i = (h - hq G) gr + t: loaded now, written at the end for the request's
+  // rows.  gr = R when the loads come before the request is read, else n.
   float g_i = 0.f, beta_i = 0.f;
-  if (tid < p.G * n) load_gate(tid % n, hq * p.G + tid / n, g_i, beta_i);
-  if (active) {
-    // channel ch of row t of the request's block
+  // channel ch: every load first, so they are all in flight together (the
+  // window oldest first, as stored)
+  T xr[RMAX], q0, q1, q2, q3, r0, r1, r2;
+  auto load_x = [&](int t) { xr[t] = static_cast<const T*>(p.x)[((size_t)b * p.R + t) * p.C + ch]; };
+  auto load_taps = [&]() {
     const T* wg = static_cast<const T*>(p.conv_w) + ch * kW;
-    T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
-    // every load first, so they are all in flight together: the current rows
-    // and (deferred) the last kWS of the previous call's rows 0..off-1
-    T xr[RMAX], xq[kWS];
+    q0 = wg[0];
+    q1 = wg[1];
+    q2 = wg[2];
+    q3 = wg[3];
+  };
+  auto load_window = [&](int sl) {
+    const T* w0 = static_cast<const T*>(p.conv_state) + ((size_t)sl * p.C + ch) * kWS;
+    r0 = w0[0];
+    r1 = w0[1];
+    r2 = w0[2];
+  };
+  if constexpr (kGuess) {  // every row the buffers hold, the taps, the guessed window; then the request
+    if (tid < p.G * p.R) load_gate(tid % p.R, hq * p.G + tid / p.R, g_i, beta_i);
+    if (active) {
 #pragma unroll
-    for (int t = 0; t < RMAX; ++t)
-      if (t < n) xr[t] = static_cast<const T*>(p.x)[((size_t)b * p.R + t) * p.C + ch];
+      for (int t = 0; t < RMAX; ++t)
+        if (t < p.R) load_x(t);
+      load_taps();
+      if (guess_ok) load_window(slot_seen);
+    }
+    t_end = request();
+    if (t_end == 0) return;
+    if (active && slot != slot_seen) load_window(slot);  // the guess missed: the request's own window
+  } else {  // the request's rows, the taps, its window
+    const int n0 = t_end - off;
+    if (tid < p.G * n0) load_gate(tid % n0, hq * p.G + tid / n0, g_i, beta_i);
+    if (active) {
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t)
+        if (t < n0) load_x(t);
+      load_taps();
+      load_window(slot);
+    }
+  }
+  const bool commit = a >= 0;
+  const int n = t_end - off;
+  const int gr = kGuess ? p.R : n;
+  if (active) {
+    T* cs = static_cast<T*>(p.conv_state) + ((size_t)slot * p.C + ch) * kWS;
+    // (deferred) the last kWS of the previous call's rows 0..off-1
+    T xq[kWS];
     if (MODE == kDeferred) {
 #pragma unroll
       for (int i = 0; i < kWS; ++i) {
@@ -572,8 +660,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
         if (t >= 0) xq[i] = static_cast<const T*>(p.xp)[((size_t)b * p.Rp + t) * p.C + ch];
       }
     }
-    const T q0 = wg[0], q1 = wg[1], q2 = wg[2], q3 = wg[3];
-    T r0 = cs[0], r1 = cs[1], r2 = cs[2];  // window, oldest first, kept as stored
     const float w0 = tof(q0), w1 = tof(q1), w2 = tof(q2), w3 = tof(q3);
     if (MODE == kDeferred) {  // the window after the previous call's rows: the one the slot commits
 #pragma unroll
@@ -728,8 +814,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     gh[i] = val;
   }
   // per-row decay and write strength of the value heads that read this q/k head
-  for (int i = tid; i < p.G * n; i += kPrepThreads) {
-    const int h = hq * p.G + i / n, t = i % n;
+  for (int i = tid; i < p.G * gr; i += kPrepThreads) {
+    const int h = hq * p.G + i / gr, t = i % gr;
+    if (t >= n) continue;
     if (i >= kPrepThreads) load_gate(t, h, g_i, beta_i);  // more (head, row) pairs than threads: load now
     float gg = g_i, bb = beta_i;
     if (p.raw_gating) {  // g = -exp(A_log) softplus(a), beta = sigmoid(b), overflow-free forms
