@@ -309,6 +309,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // declares on its barrier but never issues, so that item's wait runs out with
 // no copy in flight (-1: none).  Set by gdn_test_drop_state_copy.
 __device__ int g_test_drop_item = -1;
+// Test builds only: prologue blocks whose slot read before the wait differed
+// from the request's slot (so they loaded the window again).
+__device__ unsigned int g_test_guess_misses = 0;
+__device__ __forceinline__ void count_guess_miss() {
+  if (threadIdx.x == 0) atomicAdd(&g_test_guess_misses, 1u);
+}
+// Test builds only: a kernel ahead of a call that lets the call's grids
+// launch at once and only then, after delay_ns of %globaltimer (at most 2^22
+// polls), copies src[0..n) to dst: it rewrites the call's request data after
+// releasing it, as a producer of slot_ids may.
+__global__ void test_late_write_kernel(int* dst, const int* src, int n, unsigned long long delay_ns) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int i = 0; i < (1 << 22); ++i) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 >= delay_ns) break;
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+#else
+__device__ __forceinline__ void count_guess_miss() {}
 #endif
 
 // Validity of a request as every kernel reads it, from its n_rows n, slot and
@@ -503,6 +525,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
       t_end = request();
       if (t_end == 0) return;
       if (slot != slot_seen) {  // the guess missed: the request's own window
+        count_guess_miss();
         const Chunk* w0 = window(slot);
 #pragma unroll
         for (int i = 0; i < kWS; ++i) rc[i] = w0[i];
@@ -634,7 +657,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
     }
     t_end = request();
     if (t_end == 0) return;
-    if (active && slot != slot_seen) load_window(slot);  // the guess missed: the request's own window
+    if (slot != slot_seen) {  // the guess missed: the request's own window
+      count_guess_miss();
+      if (active) load_window(slot);
+    }
   } else {  // the request's rows, the taps, its window
     const int n0 = t_end - off;
     if (tid < p.G * n0) load_gate(tid % n0, hq * p.G + tid / n0, g_i, beta_i);
@@ -1822,6 +1848,23 @@ GDN_API int gdn_test_force_item_rows(int rows) {
   return GDN_OK;
 }
 GDN_API int gdn_test_last_item_rows() { return g_test_last_item_rows.load(std::memory_order_relaxed); }
+// Test builds only: launch the late writer on `stream` (see
+// test_late_write_kernel); read, and with reset != 0 clear, the prologue's
+// count of missed slot guesses.
+GDN_API int gdn_test_late_write(int* dst, const int* src, int n, unsigned long long delay_ns, void* stream) {
+  if (!dst || !src || n < 0) return GDN_ERR_INVALID_ARG;
+  test_late_write_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(dst, src, n, delay_ns);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+GDN_API long long gdn_test_guess_misses(int reset) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_test_guess_misses, sizeof v) != cudaSuccess) return -1;
+  if (reset) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_test_guess_misses, &z, sizeof z) != cudaSuccess) return -1;
+  }
+  return v;
+}
 #endif
 
 GDN_API const char* gdn_strerror(int code) {
