@@ -14,10 +14,11 @@
 //   the verify rows, staging [history | verify inputs] per channel [FreeToken
 //   #844 "MTP drafts for Qwen3.5 family + Flash-Next", Design / Flash-Next
 //   target verify].  Before its dependency wait it only issues L2 hints for
-//   its own inputs.
+//   its own inputs and reads the request's slot as a guess for its window.
 //
 // rows_kernel (persistent; item = (request, value head, slice of DVS state
-//   rows)): the slice of the fp32 state S (DVS x d_k, d_k contiguous) arrives
+//   rows), DVS = 32, 16 at d_k = 16, or 64 in the four-warp geometry chosen
+//   for long requests): the slice of the fp32 state S (DVS x d_k, d_k contiguous) arrives
 //   by one bulk async copy, issued for the first item before the kernel waits
 //   on the prologue, and moves to registers; the item's q, k, v and tables
 //   are staged from the work buffer by bulk async copies.  It runs the gated
