@@ -53,7 +53,9 @@
  * caller; the library keeps none after a call returns, allocates nothing,
  * and never synchronises the stream.  Calls are asynchronous on `stream`
  * (a cudaStream_t; NULL = the legacy default stream).  Active requests must
- * use distinct slots; two calls that touch the same slots or the same work
+ * use distinct slots (otherwise their results are undefined; the library's
+ * debug/test build checks this and sets GDN_STATUS_DUPLICATE_SLOT, the
+ * regular build spends nothing on it); two calls that touch the same slots or the same work
  * buffer must not run concurrently.  Each call is two kernel launches (a
  * prologue and the rows) chained with programmatic dependent launch; the
  * prologue waits for whatever ran before it on the stream.  The rows kernel
@@ -104,8 +106,10 @@ enum {
   GDN_STATUS_BAD_SLOT = 1,   /* slot outside [0, pool_slots): request skipped         */
   GDN_STATUS_BAD_NROWS = 2,  /* n_rows outside [0, R]: request skipped                */
   GDN_STATUS_BAD_ACCEPT = 4, /* accept_len outside [0, n_rows-1]: commit skipped      */
-  GDN_STATUS_TIMEOUT = 8     /* a staging copy did not complete within the kernel's
+  GDN_STATUS_TIMEOUT = 8,    /* a staging copy did not complete within the kernel's
                                 bounded wait: that block wrote nothing                */
+  GDN_STATUS_DUPLICATE_SLOT = 16 /* debug/test builds only: two active requests name
+                                the same slot (their results are undefined)           */
 };
 enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
 /* flags: GDN_FLAG_RAW_GATING - g and beta hold a layer's raw gating

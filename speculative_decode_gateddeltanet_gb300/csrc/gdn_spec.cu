@@ -469,6 +469,22 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
   if (p.early) pdl_trigger();
   pdl_wait();  // whatever ran before on the stream is complete and visible
   if (!p.early) pdl_trigger();
+#ifdef GDN_TEST_HOOKS
+  // Debug/test builds: active requests must name distinct slots.  Block x = 0
+  // of each request compares its slot with every other active request's.
+  if (blockIdx.x == 0) {
+    auto active_req = [&](int j) {
+      const int nj = p.n_rows[j];
+      return (nj > 0 && nj <= p.R) || (MODE == kDeferred && p.n_prev != nullptr && p.n_prev[j] > 0);
+    };
+    const int b0 = blockIdx.y, s0 = p.slot_ids[b0];
+    bool dup = false;
+    if (s0 >= 0 && s0 < p.P && active_req(b0))
+      for (int j = threadIdx.x; j < p.B; j += blockDim.x)
+        if (j != b0 && p.slot_ids[j] == s0 && active_req(j)) dup = true;
+    if (__syncthreads_or(dup) && threadIdx.x == 0) flag(p.status, GDN_STATUS_DUPLICATE_SLOT);
+  }
+#endif
   __shared__ float sy[RMAX][kPrepThreads];  // q/k blocks: conv outputs, [row][q | k]
 
   const int b = blockIdx.y;

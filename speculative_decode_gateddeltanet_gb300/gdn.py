@@ -16,6 +16,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libgdnspec.so"
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_LAUNCH, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
 STATIC_WORK_BYTES = 32 << 20
 STATUS_BAD_SLOT, STATUS_BAD_NROWS, STATUS_BAD_ACCEPT, STATUS_TIMEOUT = 1, 2, 4, 8
+STATUS_DUPLICATE_SLOT = 16  # debug/test builds only
 BF16, F32 = 0, 1
 FLAG_RAW_GATING = 1
 FLAG_STATE_STABLE = 2  # caller's promise: nothing still running writes this call's slots, slot_ids, n_rows

@@ -260,3 +260,15 @@ def test_carry_bytes(cuda_lib):
     assert cuda_lib.carry_bytes(good_args(cuda_lib, R=5)) == 4 * (B * 5 * (Hv * dv + Hq * dk) + B * Hv * 8)
     assert cuda_lib.carry_bytes(good_args(cuda_lib, d_k=96)) == 0
     assert cuda_lib._lib.gdn_carry_bytes(None) == 0
+
+
+def test_status_bits_match_header(cuda_lib):
+    """The binding's status constants are the header's enum values."""
+    import re
+
+    text = HEADER.read_text()
+    bits = {m.group(1): int(m.group(2)) for m in re.finditer(r"GDN_(STATUS_[A-Z_]+)\s*=\s*(\d+)", text)}
+    assert bits, "no status bits in the header"
+    for name, value in bits.items():
+        assert getattr(cuda_lib, name) == value, name
+    assert len(set(bits.values())) == len(bits), "status bits overlap"
