@@ -150,12 +150,27 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CUDA arm
-def build_stack(layers: int, device: str, batch: int | None = None, workload: str = "stack"):
+def layer_footprint(spec) -> int:
+    """Bytes of distinct device data one layer call touches: its requests'
+    state slices and conv windows (read and written in place), x, g, beta, o,
+    the taps and the work buffer."""
+    e = spec.elem_bytes
+    state = spec.B * spec.H_v * spec.d_v * spec.d_k * 4
+    conv = spec.B * spec.C * (spec.W - 1) * e + spec.C * spec.W * e
+    rows = spec.B * spec.R * (spec.C * e + spec.H_v * 8 + spec.H_v * spec.d_v * 4)
+    work = 4 * spec.B * spec.R * (2 * spec.H_qk * spec.d_k + spec.H_v * spec.d_v + 4 * spec.H_v)
+    return state + conv + rows + work
+
+
+def l2_bytes(device) -> int:
+    props = torch.cuda.get_device_properties(device)
+    return int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+
+
+def workload_specs(layers: int, batch: int | None = None, workload: str = "stack"):
+    """(LayerSpec, seed) of each layer call of one step of the workload."""
     from dataclasses import replace
 
-    from speculative_decode_gateddeltanet_gb300 import gdn
-
-    host, devs = [], []
     if workload == "ragged":  # B=256 requests of 2, 4 or 9 rows, 64 value heads, 10 % inactive
         base = CONFIGS[RAGGED]
         specs = [(replace(base, name=f"ragged-{layers}L-B256-k1_3_8"), 4000 + i) for i in range(layers)]
@@ -169,9 +184,19 @@ def build_stack(layers: int, device: str, batch: int | None = None, workload: st
         batch = None
     else:
         specs = workload_layers(STACK, layers=layers)
+    out = []
     for spec, seed in specs:
         if batch is not None and batch != spec.B:
             spec = replace(spec, B=batch, name=f"qwen35-{layers}L-B{batch}-k{spec.k}")
+        out.append((spec, seed))
+    return out
+
+
+def build_stack(layers: int, device: str, batch: int | None = None, workload: str = "stack"):
+    from speculative_decode_gateddeltanet_gb300 import gdn
+
+    host, devs = [], []
+    for spec, seed in workload_specs(layers, batch, workload):
         layer = make_layer(spec, seed)
         host.append(layer)
         devs.append(gdn.DeviceLayer(layer, device, snapshot=False))
@@ -186,6 +211,13 @@ def run_cuda(args, rank, ws, local):
 
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
+    if args.layers is None:
+        # The workload's default layer count, raised until the distinct data one step touches is at
+        # least twice the L2: the timed steps then cannot find earlier steps' data in L2.
+        default = 4 if args.workload == "ragged" else 36
+        probe = workload_specs(1, args.batch, args.workload)[0][0]
+        need = -(-2 * l2_bytes(device) // layer_footprint(probe))
+        args.layers = max(default, need)
     host, devs = build_stack(args.layers, device, args.batch, args.workload)
     spec = host[0]["spec"]
     if args.mode == "snapshot":
@@ -363,8 +395,10 @@ def run_cuda(args, rank, ws, local):
                    "d_v": spec.d_v, "storage": "bf16 x/conv, fp32 g/beta/state/o", "mode": args.mode,
                    "launch": "cuda graph replay" if args.graph else "stream launches",
                    "state_stable": bool(args.stable),
-                   "l2": "inputs larger than L2: each step streams %.2f GB over %d distinct layers"
-                         % (bytes_per_step / 1e9, len(cargs))},
+                   "l2": "inputs larger than L2: each step touches %.0f MB of distinct data (%d layers; "
+                         "L2 %.0f MB) and streams %.2f GB"
+                         % (sum(layer_footprint(h["spec"]) for h in host) / 1e6, len(cargs),
+                            l2_bytes(device) / 1e6, bytes_per_step / 1e9)},
         "hbm_gbs": round(bytes_per_step * ws / (ms_step / 1e3) / 1e9, 1),
         "bytes_per_row": round(bytes_per_step / rows_per_step),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -576,8 +610,6 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.layers is None:
-        args.layers = 4 if args.workload == "ragged" else 36
     rank, ws, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, ws)
