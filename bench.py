@@ -426,7 +426,7 @@ def run_cuda(args, rank, ws, local):
 def run_accept(args, rank, ws, local):
     """Device-side greedy acceptance on the verify shape: B=16 requests of
     4 rows over the 151936-token vocabulary in bf16, L distinct calls per
-    step (inputs larger than L2 across the step)."""
+    step (a step's logits at least twice the L2)."""
     from speculative_decode_gateddeltanet_gb300 import build as pkg_build
     from speculative_decode_gateddeltanet_gb300.inputs import make_accept_case
 
@@ -435,7 +435,9 @@ def run_accept(args, rank, ws, local):
 
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    B, R, V, L = 16, 4, 151936, 12
+    B, R, V = 16, 4, 151936
+    # enough distinct calls that a step's logits (19.4 MB per call) are at least twice the L2
+    L = max(12, -(-2 * l2_bytes(device) // (B * R * V * 2)))
     calls = []
     for i in range(L):
         c = make_accept_case(B, R, V, seed=9000 + i)
