@@ -436,14 +436,19 @@ def run_accept(args, rank, ws, local):
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
     B, R, V = 16, 4, 151936
-    # enough distinct calls that a step's logits (19.4 MB per call) are at least twice the L2
-    L = max(12, -(-2 * l2_bytes(device) // (B * R * V * 2)))
-    calls = []
-    for i in range(L):
+    # enough distinct calls (at least 12) that the logits a step reads (its valid rows') are at
+    # least twice the L2
+    need = 2 * l2_bytes(device)
+    calls, read = [], 0
+    i = 0
+    while len(calls) < 12 or read < need:
         c = make_accept_case(B, R, V, seed=9000 + i)
         calls.append({k: c[k].to(device) for k in ("logits", "drafts", "n_rows")}
                      | {"target": torch.empty((B, R), dtype=torch.int32, device=device),
                         "acc": torch.empty(B, dtype=torch.int32, device=device)})
+        read += int(c["n_rows"].sum()) * V * 2
+        i += 1
+    L = len(calls)
     rows = sum(int(c["n_rows"].sum()) for c in calls)
     nbytes = sum(int(c["n_rows"].sum()) * V * 2 for c in calls)  # the valid rows' logits, read once
     stream = torch.cuda.Stream(device)
@@ -456,6 +461,9 @@ def run_accept(args, rank, ws, local):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.4)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     ev0.record(stream)
@@ -465,6 +473,7 @@ def run_accept(args, rank, ws, local):
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
+    clocks = sampler.stop() if sampler else None
     ms_step = max_over_ranks(ev0.elapsed_time(ev1), ws) / args.steps
     peak, peak_kind = hbm_peak()
     gbs = nbytes / (ms_step / 1e3) / 1e9
@@ -478,7 +487,7 @@ def run_accept(args, rank, ws, local):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
                          "kernel": "argmax_kernel<bf16> + accept_kernel", "traffic": None},
-            "gpu_launches": 2 * L * args.steps}
+            "gpu_launches": 2 * L * args.steps, "clocks": clocks}
 
 
 # ------------------------------------------------------------ oracle arm
